@@ -1,0 +1,131 @@
+"""Seeded synthetic inputs for causal attention, shared by the CUDA path's tests,
+the benchmark and the oracle's tests.
+
+This module holds no attention arithmetic: it only names the workloads and
+draws their Q, K, V and dO tensors on the CPU from a seeded torch generator,
+rounded to the workload's storage dtype. Everything that consumes the tensors
+(the CUDA path, the fp64 oracle) receives the same rounded values.
+
+Workloads (shapes in [B, H, S, d] order, Q/dO with Hq heads, K/V with Hkv):
+
+  tiny_fp32    fp32,  B=1 Hq=Hkv=2  S=128   d=64,  N(0,1), seed 0
+  gpt2_small   bf16,  B=8 Hq=Hkv=12 S=1024  d=64,  N(0,1), seed 1
+  gqa_qwen3    bf16,  B=4 Hq=32 Hkv=8 S=2048 d=128, N(0,1), seed 2
+  long_8k      bf16,  B=1 Hq=Hkv=32 S=8192  d=128, 0.5*N(0,1) with every
+               512th key (positions 0, 512, 1024, ...) scaled by 8, seed 3
+  fp16_32k     fp16,  B=1 Hq=Hkv=8  S=32768 d=64,  N(0,1), seed 4, forward only
+
+All use causal masking and scale = 1/sqrt(d).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+DTYPES = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    d: int
+    seed: int
+    causal: bool = True
+    backward: bool = True
+    value_scale: float = 1.0      # multiplies every N(0,1) draw
+    spike_every: int = 0          # if > 0: K rows at positions % spike_every == 0 ...
+    spike_scale: float = 1.0      # ... are multiplied by this before rounding
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    def describe(self) -> str:
+        s = (f"{self.name}: {self.dtype} B={self.B} Hq={self.Hq} Hkv={self.Hkv} "
+             f"S={self.S} d={self.d} causal={int(self.causal)} seed={self.seed}")
+        if self.value_scale != 1.0:
+            s += f" values={self.value_scale}*N(0,1)"
+        if self.spike_every:
+            s += f" K[j]*={self.spike_scale} for j%{self.spike_every}==0"
+        return s
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_fp32", "fp32", 1, 2, 2, 128, 64, seed=0),
+        Workload("gpt2_small", "bf16", 8, 12, 12, 1024, 64, seed=1),
+        Workload("gqa_qwen3", "bf16", 4, 32, 8, 2048, 128, seed=2),
+        Workload("long_8k", "bf16", 1, 32, 32, 8192, 128, seed=3,
+                 value_scale=0.5, spike_every=512, spike_scale=8.0),
+        Workload("fp16_32k", "fp16", 1, 8, 8, 32768, 64, seed=4, backward=False),
+    ]
+}
+
+
+def make_inputs(w: Workload, with_dout: bool = True):
+    """Draw (q, k, v[, dout]) on the CPU for workload `w`.
+
+    Draw order is Q, K, V, dO from one generator seeded with `w.seed`; each
+    tensor is drawn in fp32, multiplied by `value_scale`, K gets its spike
+    rows, and the result is rounded (round-to-nearest-even) to the storage
+    dtype.
+    """
+    g = torch.Generator().manual_seed(w.seed)
+    qshape = (w.B, w.Hq, w.S, w.d)
+    kshape = (w.B, w.Hkv, w.S, w.d)
+
+    def draw(shape):
+        t = torch.randn(shape, generator=g, dtype=torch.float32)
+        if w.value_scale != 1.0:
+            t.mul_(w.value_scale)
+        return t
+
+    q = draw(qshape)
+    k = draw(kshape)
+    if w.spike_every:
+        k[:, :, :: w.spike_every, :] *= w.spike_scale
+    v = draw(kshape)
+    out = [q, k, v]
+    if with_dout:
+        out.append(draw(qshape))
+    return tuple(t.to(w.torch_dtype) for t in out)
+
+
+def make_custom(B, Hq, Hkv, S, d, dtype="bf16", seed=0, value_scale=1.0,
+                with_dout=True):
+    """Same recipe as `make_inputs` for an ad-hoc shape (edge-case tests)."""
+    w = Workload("custom", dtype, B, Hq, Hkv, S, d, seed=seed,
+                 value_scale=value_scale)
+    return make_inputs(w, with_dout=with_dout)
+
+
+def sample_rows(S: int, n: int, seed: int, tile: int = 128):
+    """Sorted distinct row indices for sampled checks at long S.
+
+    Always contains 0, S-1 and the tile boundaries tile-1/tile and
+    2*tile-1/2*tile (plus 511/512 when S is large enough), the rest drawn
+    uniformly from a seeded generator.
+    """
+    must = {0, S - 1}
+    for t in (tile, 2 * tile, 512):
+        if t < S:
+            must.update({t - 1, t})
+    rows = set(must)
+    g = torch.Generator().manual_seed(seed)
+    for r in torch.randperm(S, generator=g).tolist():
+        if len(rows) >= n:
+            break
+        rows.add(r)
+    return sorted(rows)
