@@ -1,0 +1,159 @@
+"""Causal flash attention on one NVIDIA GB300 (sm_103a): thin Python binding of
+libfa (include/fa.h).
+
+The functions with the C names (`fa_fwd`, `fa_bwd`, `fa_bwd_workspace_bytes`,
+`fa_strerror`, `fa_last_device_status`, `fa_version`) only marshal arguments:
+shapes come from the tensors, pointers from `data_ptr()`, and the stream from
+PyTorch's current stream. Every step of the computation runs in libfa's CUDA
+kernels; there is no other code path. `attention_forward` / `attention_backward`
+additionally allocate their outputs (and the backward workspace) with
+PyTorch.
+
+The library is built in-tree by `causal_flash_attention_gb300.build.build()`;
+loading it raises if it has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_strerror",
+    "fa_last_device_status", "fa_version", "attention_forward", "attention_backward",
+    "DTYPE_CODES",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {fa_strerror(code)} (code {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (once) and declare its C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with causal_flash_attention_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+    L.fa_fwd.restype = i32
+    L.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.fa_bwd_workspace_bytes.restype = sz
+    L.fa_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    L.fa_bwd.restype = i32
+    L.fa_strerror.argtypes = [i32]
+    L.fa_strerror.restype = ctypes.c_char_p
+    L.fa_last_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+    L.fa_last_device_status.restype = i32
+    L.fa_version.argtypes = []
+    L.fa_version.restype = i32
+    _lib = L
+    return L
+
+
+def fa_strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def fa_version() -> int:
+    return int(lib().fa_version())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, H, S, d]")
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    return int(B), int(Hq), int(Hkv), int(S), int(d)
+
+
+def _check_contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def fa_fwd(q, k, v, out, lse, causal=True, scale=None, stream=None):
+    """Call fa_fwd on caller-provided tensors (out: like q; lse: float32 [B,Hq,S])."""
+    _check_contig(q, k, v, out, lse)
+    B, Hq, Hkv, S, d = _dims(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, d,
+                      int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, Hq, Hkv, S, d))
+
+
+def fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale=None,
+           stream=None):
+    """Call fa_bwd on caller-provided tensors; `workspace` is a device tensor of at
+    least fa_bwd_workspace_bytes(...) bytes."""
+    _check_contig(q, k, v, out, dout, lse, dq, dk, dv)
+    B, Hq, Hkv, S, d = _dims(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                      _ptr(dk), _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale,
+                      DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes, _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_bwd")
+
+
+def fa_last_device_status(stream=None) -> int:
+    st = ctypes.c_int(0)
+    rc = lib().fa_last_device_status(_stream(stream), ctypes.byref(st))
+    if rc != 0:
+        raise FAError(rc, "fa_last_device_status")
+    return st.value
+
+
+def attention_forward(q, k, v, causal=True, scale=None, stream=None):
+    """Allocate out and lse with PyTorch and run fa_fwd. Returns (out, lse)."""
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, out, lse, causal, scale, stream)
+    return out, lse
+
+
+def workspace_for(q, k):
+    B, Hq, Hkv, S, d = _dims(q, k)
+    n = fa_bwd_workspace_bytes(B, Hq, Hkv, S, d)
+    return torch.empty(n, dtype=torch.uint8, device=q.device)
+
+
+def attention_backward(q, k, v, out, dout, lse, causal=True, scale=None, workspace=None,
+                       stream=None):
+    """Allocate dq, dk, dv (and a workspace unless given) and run fa_bwd."""
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = workspace_for(q, k)
+    fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    return dq, dk, dv

@@ -1,0 +1,251 @@
+// C-ABI entry points of libfa (declared in include/fa.h): argument checks,
+// TMA descriptor construction and kernel launches. No device memory is
+// allocated here; the only device-resident state is the status word below.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// Sticky device status word: kernels OR kStatus* bits into it when they give
+// up a wait instead of hanging.
+__device__ int g_status;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+int* status_ptr() {
+  int* p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status) != cudaSuccess) return nullptr;
+  return p;
+}
+
+// 3-D view [rows = BH][S][d] of a contiguous 16-bit tensor; box = 64 columns
+// (128 bytes, one swizzle span) x 128 sequence rows x 1 head.
+bool make_tmap(CUtensorMap* m, const void* base, int BH, int S, int d, bool bf16) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(S) * d * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kTileM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int Hq, int Hkv, int S, int d, float scale, int dtype) {
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_SHAPE;
+  // grid and index ranges: B*Hq*ceil(S/256) CTAs, element offsets in 64 bits
+  const long long bh = static_cast<long long>(B) * Hq;
+  if (bh > (1LL << 30) || S > (1 << 30) || bh * ((S + 255) / 256) > 0x7fffffffLL)
+    return FA_ERR_SHAPE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_SCALE;
+  return FA_OK;
+}
+
+inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+struct WsLayout {
+  size_t dq_acc, delta, lse2, total;
+};
+
+WsLayout ws_layout(int B, int Hq, int S, int d) {
+  const long long bh = static_cast<long long>(B) * Hq;
+  const long long s_pad = round_up(S, kTileM);
+  WsLayout w;
+  w.dq_acc = 0;
+  w.delta = static_cast<size_t>(round_up(bh * s_pad * d * 4, 256));
+  w.lse2 = w.delta + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
+  w.total = w.lse2 + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
+  return w;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_SHAPE: return "invalid shape (B, Hq, Hkv, S >= 1, Hq % Hkv == 0, d in {64, 128})";
+    case FA_ERR_DTYPE: return "unsupported dtype (FA_F32, FA_F16 or FA_BF16)";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_bwd_workspace_bytes()";
+    case FA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case FA_ERR_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_TMA: return "the driver rejected a tensor-memory-access descriptor";
+    default: return "unknown error code";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+           int Hkv, int S, int d, int causal, float scale, int dtype, fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, S, d, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  if (dtype == FA_F32) {
+    SimtParams p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.o_out = static_cast<float*>(out);
+    p.lse_out = lse;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.d = d;
+    p.causal = causal != 0;
+    p.scale = scale;
+    return launch_fwd_simt(p, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  const bool bf16 = dtype == FA_BF16;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tm_q, q, B * Hq, S, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, S, d, bf16) ||
+      !make_tmap(&p.tm_v, v, B * Hkv, S, d, bf16))
+    return FA_ERR_TMA;
+  p.out = out;
+  p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S;
+  p.causal = causal != 0;
+  p.scale_log2 = scale * kLog2e;
+  p.n_qpairs = (S + 2 * kTileM - 1) / (2 * kTileM);
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  return launch_fwd_tc(p, d, bf16, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int S, int d) {
+  if (check_common(B, Hq, Hkv, S, d, 1.f, FA_BF16) != FA_OK) return 0;
+  return ws_layout(B, Hq, S, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int d,
+           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, S, d, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGN;
+  const WsLayout ws = ws_layout(B, Hq, S, d);
+  if (!workspace || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  const int BH = B * Hq;
+  const int S_pad = static_cast<int>(round_up(S, kTileM));
+
+  BwdPreParams pre;
+  pre.out = out;
+  pre.dout = dout;
+  pre.lse = lse;
+  pre.delta = reinterpret_cast<float*>(wsb + ws.delta);
+  pre.lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  pre.dq_acc = dtype == FA_F32 ? nullptr : reinterpret_cast<float*>(wsb + ws.dq_acc);
+  pre.BH = BH; pre.S = S; pre.S_pad = S_pad; pre.d = d;
+  pre.dtype = dtype;
+  if (launch_bwd_pre(pre, st) != cudaSuccess) return FA_ERR_CUDA;
+
+  if (dtype == FA_F32) {
+    SimtParams p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.dout = static_cast<const float*>(dout);
+    p.lse = lse;
+    p.delta = pre.delta;
+    p.dq = static_cast<float*>(dq);
+    p.dk = static_cast<float*>(dk);
+    p.dv = static_cast<float*>(dv);
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.d = d;
+    p.causal = causal != 0;
+    p.scale = scale;
+    return launch_bwd_simt(p, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  const bool bf16 = dtype == FA_BF16;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tm_q, q, BH, S, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, S, d, bf16) ||
+      !make_tmap(&p.tm_v, v, B * Hkv, S, d, bf16) || !make_tmap(&p.tm_do, dout, BH, S, d, bf16))
+    return FA_ERR_TMA;
+  p.delta = pre.delta;
+  p.lse2 = pre.lse2;
+  p.dq_acc = pre.dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.S_pad = S_pad;
+  p.causal = causal != 0;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.n_kv_tiles = (S + kTileN - 1) / kTileN;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  if (launch_bwd_tc(p, d, bf16, st) != cudaSuccess) return FA_ERR_CUDA;
+
+  DqConvertParams cv;
+  cv.dq_acc = pre.dq_acc;
+  cv.dq = dq;
+  cv.BH = BH; cv.S = S; cv.S_pad = S_pad; cv.d = d;
+  cv.scale = scale;
+  cv.dtype = dtype;
+  return launch_dq_convert(cv, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_last_device_status(fa_stream_t stream, int* status) {
+  if (!status) return FA_ERR_NULL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int value = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&value, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  *status = value;
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,523 @@
+// Backward pass of causal flash attention on sm_103a.
+//
+// Follows the recomputation scheme of "Phase T14: 融合 Flash-Attention
+// Kernel", section 什么是 flash-attention (backward formulas) and its Key
+// Design Decisions item 3: with D_i = <dO_i, O_i>,
+//   p_ij = exp(s_ij - L_i), dp_ij = <dO_i, V_j>, ds_ij = p_ij (dp_ij - D_i),
+//   dQ_i = scale sum_j ds_ij K_j, dK_j = scale sum_i ds_ij Q_i, dV_j = sum_i p_ij dO_i.
+//
+// Three kernels on one stream:
+//   1. bwd_pre:    D_i, L_i * log2(e) (padded rows: D = 0, L = +inf) and a zeroed
+//                  fp32 dQ accumulator. Bandwidth-bound.
+//   2. bwd_main:   one CTA per (batch, key/value head, 128-row key tile j). K_j and
+//                  V_j stay in shared memory, dK_j and dV_j stay in tensor memory
+//                  for the whole CTA (so no atomics for them), and the CTA walks
+//                  every query tile i >= j (causal) of every query head of the
+//                  group. Per step, on the tensor cores:
+//                    S^T  = K_j Q_i^T          -> TMEM (kv rows x q cols)
+//                    dP^T = V_j dO_i^T         -> TMEM
+//                    [softmax warps: P^T = 2^(S^T*c - L*log2e), masked; written as
+//                     16-bit into TMEM; dS^T = P^T (dP^T - D) written to smem]
+//                    dV  += P^T dO_i           (P^T from TMEM)
+//                    dK  += dS^T Q_i
+//                    dQ   = dS K_j             -> TMEM, then added (fp32 vector
+//                                                 atomics) into the dQ accumulator
+//   3. dq_convert: dq = scale * accumulator, rounded to the input type.
+//
+// Warp roles of bwd_main (320 threads): warp 0 TMA producer (K_j, V_j once;
+// Q_i, dO_i, L_i, D_i through a 2-stage ring), warp 1 MMA issuer and TMEM
+// owner, warps 2-5 compute P^T and dS^T (one thread per key row), warps 6-9
+// move dQ from TMEM to the global accumulator (one thread per query row);
+// at the end warps 2-5 write dK and warps 6-9 write dV.
+//
+// Tensor memory: dK [0,d), dV [128,128+d), S^T / P^T [256,384),
+// dP^T / dQ [384,512). dQ reuses dP^T's columns once the softmax warps have
+// read dP^T; S^T(i+1) is issued only after dV(i), which reads P^T(i), is done.
+#include <algorithm>
+#include <type_traits>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 320;
+constexpr float kLog2eF = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / kChunk;
+  static constexpr int kTileBytes = kTileM * D * 2;        // one 128 x D tile
+  static constexpr int kStages = (D == 128) ? 2 : 3;       // Q/dO ring depth
+  static constexpr int kDsBytes = kTileN * kTileM * 2;     // dS^T, 128 x 128 16-bit
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;                 // [stages]
+  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // [stages]
+  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
+  static constexpr int kOffRow = kOffDS + kDsBytes;                // [stages] x (L2 | D) x 128 f32
+  static constexpr int kOffBar = kOffRow + kStages * 1024;
+  // kv_full, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_full,
+  // dv_done, dq_full, dq_empty, ds_empty, kd_done, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 10;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(status, kStatusWaitTimeout);
+      return;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// ------------------------------------------------------------------ pre --
+// One warp per (head row, sequence row) in [0, S_pad): D = <dO, O> in fp32,
+// L*log2(e), and a zeroed dQ accumulator row.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // bh * S_pad + i
+  if (row >= static_cast<long long>(p.BH) * p.S_pad) return;
+  const int bh = static_cast<int>(row / p.S_pad), i = static_cast<int>(row % p.S_pad);
+  float dsum = 0.f;
+  if (i < p.S) {
+    const size_t off = (static_cast<size_t>(bh) * p.S + i) * p.d;
+    const T* o = static_cast<const T*>(p.out) + off;
+    const T* g = static_cast<const T*>(p.dout) + off;
+    for (int e = lane; e < p.d; e += 32) dsum = fmaf(to_f(o[e]), to_f(g[e]), dsum);
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+  if (lane == 0) {
+    p.delta[row] = (i < p.S) ? dsum : 0.f;
+    p.lse2[row] = (i < p.S) ? p.lse[static_cast<size_t>(bh) * p.S + i] * kLog2eF : INFINITY;
+  }
+  if (p.dq_acc) {
+    float4* acc = reinterpret_cast<float4*>(p.dq_acc + static_cast<size_t>(row) * p.d);
+    for (int e = lane; e < p.d / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// -------------------------------------------------------------- convert --
+// dq = scale * dq_acc (rows < S), 8 elements per thread.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
+  const long long n8 = static_cast<long long>(p.BH) * p.S * p.d / 8;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long e = t * 8;
+    const long long rowd = e / p.d;                      // bh * S + i
+    const int col = static_cast<int>(e % p.d);
+    const long long bh = rowd / p.S, i = rowd % p.S;
+    const float4* src =
+        reinterpret_cast<const float4*>(p.dq_acc + (bh * p.S_pad + i) * p.d + col);
+    const float4 a = src[0], b = src[1];
+    uint4 w;
+    w.x = pack2<kBf16>(a.x * p.scale, a.y * p.scale);
+    w.y = pack2<kBf16>(a.z * p.scale, a.w * p.scale);
+    w.z = pack2<kBf16>(b.x * p.scale, b.y * p.scale);
+    w.w = pack2<kBf16>(b.z * p.scale, b.w * p.scale);
+    reinterpret_cast<uint4*>(p.dq)[t] = w;
+  }
+}
+
+// ----------------------------------------------------------------- main --
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  constexpr int NS = Cfg::kStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {   // the 128-byte swizzle needs 1024-byte aligned tiles
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadLaunch);
+    return;
+  }
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  const uint32_t kv_full = bar0;
+  auto qdo_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto qdo_empty = [&](int s) { return bar0 + 8 * (1 + NS + s); };
+  const uint32_t s_full = bar0 + 8 * (1 + 2 * NS);
+  const uint32_t dp_full = s_full + 8;
+  const uint32_t p_full = s_full + 16;
+  const uint32_t ds_full = s_full + 24;
+  const uint32_t dv_done = s_full + 32;
+  const uint32_t dq_full = s_full + 40;
+  const uint32_t dq_empty = s_full + 48;
+  const uint32_t ds_empty = s_full + 56;
+  const uint32_t kd_done = s_full + 64;
+  const uint32_t drain = s_full + 72;
+
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+
+  // ---- work: key tile j of (batch, kv head); small j first (most query tiles) ----
+  const int BHkv = p.B * p.Hkv;
+  const int j = static_cast<int>(blockIdx.x) / BHkv;
+  const int bkv = static_cast<int>(blockIdx.x) % BHkv;
+  const int b = bkv / p.Hkv, g = bkv % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int n_qt = p.n_kv_tiles;                 // query tiles per head (same S)
+  const int i_start = p.causal ? j : 0;
+  const int n_i = n_qt - i_start;
+  const int n_iter = G * n_i;
+  auto bh_of = [&](int it) { return b * p.Hq + g * G + it / n_i; };
+  auto i_of = [&](int it) { return i_start + it % n_i; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(qdo_full(s), 1);
+      mbar_init(qdo_empty(s), 1 + 4);   // MMA commit + one per softmax warp
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(ds_full, 4);
+    mbar_init(dv_done, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 4);
+    mbar_init(ds_empty, 1);
+    mbar_init(kd_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTileBytes);
+      for (int c = 0; c < Cfg::kChunks; ++c) {
+        tma_load_3d(sbase + Cfg::kOffK + c * (kTileN * 128), &p.tm_k, kv_full, c * kChunk,
+                    j * kTileN, bkv);
+        tma_load_3d(sbase + Cfg::kOffV + c * (kTileN * 128), &p.tm_v, kv_full, c * kChunk,
+                    j * kTileN, bkv);
+      }
+      int it = 0;
+      for (; it < n_iter; ++it) {
+        const int st = it % NS;
+        const uint32_t use = static_cast<uint32_t>(it / NS);
+        if (it >= NS && !mbar_wait(qdo_empty(st), (use - 1) & 1, abort_flag, p.status)) break;
+        const int bh = bh_of(it), i = i_of(it);
+        const uint32_t fb = qdo_full(st);
+        mbar_arrive_expect_tx(fb, 2 * Cfg::kTileBytes + 1024);
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          tma_load_3d(sbase + Cfg::kOffQ + st * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_q, fb,
+                      c * kChunk, i * kTileM, bh);
+          tma_load_3d(sbase + Cfg::kOffDO + st * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_do,
+                      fb, c * kChunk, i * kTileM, bh);
+        }
+        const size_t roff = static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM;
+        bulk_load(sbase + Cfg::kOffRow + st * 1024, p.lse2 + roff, 512, fb);
+        bulk_load(sbase + Cfg::kOffRow + st * 1024 + 512, p.delta + roff, 512, fb);
+      }
+      if (*abort_flag) {
+        drain_wait(kv_full, 0, p.status);
+        for (int jj = max(0, it - NS); jj < it; ++jj)
+          drain_wait(qdo_full(jj % NS), static_cast<uint32_t>(jj / NS) & 1, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc(128, kTileM, kBf16, false, false);  // S^T, dP^T
+      constexpr uint32_t idesc_kv = make_idesc(128, D, kBf16, false, true);       // dV, dK
+      constexpr uint32_t idesc_q = make_idesc(128, D, kBf16, true, true);         // dQ
+      const uint32_t t_dk = tmem, t_dv = tmem + 128, t_s = tmem + 256, t_dp = tmem + 384;
+      const uint32_t k_s = sbase + Cfg::kOffK, v_s = sbase + Cfg::kOffV;
+      const uint32_t ds_s = sbase + Cfg::kOffDS;
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int st = it % NS;
+        const uint32_t par = static_cast<uint32_t>(it / NS) & 1;
+        const uint32_t q_s = sbase + Cfg::kOffQ + st * Cfg::kTileBytes;
+        const uint32_t do_s = sbase + Cfg::kOffDO + st * Cfg::kTileBytes;
+        if (!(ok = mbar_wait(qdo_full(st), par, abort_flag, p.status))) break;
+        if (it > 0 && !(ok = mbar_wait(dv_done, (it - 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // S^T = K_j Q_i^T
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
+          mma_ss(t_s, make_sdesc(k_s + off, 16, 1024), make_sdesc(q_s + off, 16, 1024), idesc_s,
+                 ks > 0);
+        }
+        tc_commit(s_full);
+        if (it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dP^T = V_j dO_i^T
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
+          mma_ss(t_dp, make_sdesc(v_s + off, 16, 1024), make_sdesc(do_s + off, 16, 1024), idesc_s,
+                 ks > 0);
+        }
+        tc_commit(dp_full);
+        if (!(ok = mbar_wait(p_full, it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dV += P^T dO_i  (P^T from TMEM, 16-bit packed in S^T's first 64 columns)
+#pragma unroll
+        for (int ks = 0; ks < kTileM / 16; ++ks)
+          mma_ts(t_dv, t_s + ks * 8, make_sdesc(do_s + ks * 2048, kTileM * 128, 1024), idesc_kv,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(dv_done);
+        if (!(ok = mbar_wait(ds_full, it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+        // dK += dS^T Q_i
+#pragma unroll
+        for (int ks = 0; ks < kTileM / 16; ++ks)
+          mma_ss(t_dk, make_sdesc(ds_s + (ks / 4) * (kTileN * 128) + (ks % 4) * 32, 16, 1024),
+                 make_sdesc(q_s + ks * 2048, kTileM * 128, 1024), idesc_kv,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        // dQ = dS K_j  (dS read MN-major from the same dS^T tile)
+#pragma unroll
+        for (int ks = 0; ks < kTileN / 16; ++ks)
+          mma_ss(t_dp, make_sdesc(ds_s + ks * 2048, kTileM * 128, 1024),
+                 make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
+        tc_commit(dq_full);
+        tc_commit(qdo_empty(st));
+        tc_commit(ds_empty);
+      }
+      tc_commit(ok ? kd_done : drain);
+      if (!ok) drain_wait(drain, 0, p.status);
+    }
+  } else if (warp < 6) {
+    // ===================== P^T and dS^T (one thread per key row) =====================
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int kv = j * kTileN + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + 256;
+    const uint32_t t_dp = tmem + lane_off + 384;
+    const float c = p.scale_log2;
+    uint8_t* ds_row = smem + Cfg::kOffDS + r * 128;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % NS;
+      const uint32_t par = static_cast<uint32_t>(it / NS) & 1;
+      const int i = i_of(it);
+      const float* rowv = reinterpret_cast<const float*>(smem + Cfg::kOffRow + st * 1024);
+      const float* l2s = rowv;          // L * log2(e) per query column
+      const float* dls = rowv + 128;    // D per query column
+      ok = __all_sync(0xffffffffu, mbar_wait(qdo_full(st), par, abort_flag, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      // masked: key past the end, or (causal) key after the query
+      const bool any_mask = (j * kTileN + kTileN > p.S) || (p.causal && i == j);
+      const int q0 = i * kTileM;
+      uint32_t ppk[64];
+#pragma unroll
+      for (int cc = 0; cc < kTileM / 32; ++cc) {
+        uint32_t raw[32];
+        tmem_ld32(t_s + cc * 32, raw);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int qc = cc * 32 + e;
+          float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[qc]));
+          float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[qc + 1]));
+          if (any_mask) {
+            if (kv >= p.S || (p.causal && kv > q0 + qc)) p0 = 0.f;
+            if (kv >= p.S || (p.causal && kv > q0 + qc + 1)) p1 = 0.f;
+          }
+          ppk[cc * 16 + e / 2] = pack2<kBf16>(p0, p1);
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = ppk[cc * 16 + e];
+        tmem_st16(t_s + cc * 16, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+
+      if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (it - 1) & 1, abort_flag, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < kTileM / 32; ++cc) {
+        uint32_t raw[32];
+        tmem_ld32(t_dp + cc * 32, raw);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int qc = cc * 32 + e;
+          const float2 pp = unpack2<kBf16>(ppk[cc * 16 + e / 2]);
+          const float d0 = pp.x * (__uint_as_float(raw[e]) - dls[qc]);
+          const float d1 = pp.y * (__uint_as_float(raw[e + 1]) - dls[qc + 1]);
+          w[e / 2] = pack2<kBf16>(d0, d1);
+        }
+        // 128-byte swizzle: 16-byte unit u of row r sits at unit u ^ (r % 8)
+        uint8_t* chunk_row = ds_row + (cc / 2) * (kTileN * 128);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int u = (cc % 2) * 4 + v;
+          *reinterpret_cast<uint4*>(chunk_row + ((u ^ (r & 7)) << 4)) =
+              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(ds_full);
+        mbar_arrive(qdo_empty(st));
+      }
+    }
+    // ---- epilogue: dK = scale * accumulated dS^T Q ----
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
+    if (ok) {
+      tc_fence_after();
+      using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
+      Elem* dst = reinterpret_cast<Elem*>(p.dk) + (static_cast<size_t>(bkv) * p.S + kv) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + cc * 32, o);
+        tmem_wait_ld();
+        if (kv < p.S) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            d4[v] = make_uint4(
+                pack2<kBf16>(__uint_as_float(o[8 * v]) * p.scale, __uint_as_float(o[8 * v + 1]) * p.scale),
+                pack2<kBf16>(__uint_as_float(o[8 * v + 2]) * p.scale, __uint_as_float(o[8 * v + 3]) * p.scale),
+                pack2<kBf16>(__uint_as_float(o[8 * v + 4]) * p.scale, __uint_as_float(o[8 * v + 5]) * p.scale),
+                pack2<kBf16>(__uint_as_float(o[8 * v + 6]) * p.scale, __uint_as_float(o[8 * v + 7]) * p.scale));
+        }
+      }
+    }
+  } else {
+    // ===================== dQ: TMEM -> fp32 accumulator (one thread per query row) ====
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_dq = tmem + lane_off + 384;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t raw[32];
+        tmem_ld32(t_dq + cc * 32, raw);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[cc * 32 + e] = raw[e];
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+      const int bh = bh_of(it), i = i_of(it);
+      float4* dst = reinterpret_cast<float4*>(
+          p.dq_acc + (static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM + r) * D);
+#pragma unroll
+      for (int v = 0; v < D / 4; ++v)
+        atomicAdd(dst + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                       __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
+    }
+    // ---- epilogue: dV ----
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
+    if (ok) {
+      tc_fence_after();
+      const int kv = j * kTileN + r;
+      using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
+      Elem* dst = reinterpret_cast<Elem*>(p.dv) + (static_cast<size_t>(bkv) * p.S + kv) * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + 128 + cc * 32, o);
+        tmem_wait_ld();
+        if (kv < p.S) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            d4[v] = make_uint4(pack2<kBf16>(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
+                               pack2<kBf16>(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
+                               pack2<kBf16>(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
+                               pack2<kBf16>(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
+  constexpr int smem = BwdCfg<D>::kSmemBytes;
+  auto kernel = fa_bwd_kernel<D, kBf16>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.n_kv_tiles * p.B * p.Hkv);
+  kernel<<<grid, kBwdThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.BH) * p.S_pad;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  if (p.dtype == 0) bwd_pre_kernel<float><<<grid, 256, 0, stream>>>(p);
+  else if (p.dtype == 1) bwd_pre_kernel<__half><<<grid, 256, 0, stream>>>(p);
+  else bwd_pre_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_tc(const BwdParams& p, int d, bool bf16, cudaStream_t stream) {
+  if (d == 128) return bf16 ? launch_bwd_impl<128, true>(p, stream) : launch_bwd_impl<128, false>(p, stream);
+  return bf16 ? launch_bwd_impl<64, true>(p, stream) : launch_bwd_impl<64, false>(p, stream);
+}
+
+cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(p.BH) * p.S * p.d / 8;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>((n8 + 255) / 256, 152LL * 16));
+  if (p.dtype == 2) dq_convert_kernel<true><<<grid, 256, 0, stream>>>(p);
+  else dq_convert_kernel<false><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

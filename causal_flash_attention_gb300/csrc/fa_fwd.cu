@@ -1,0 +1,423 @@
+// Forward pass of causal scaled-dot-product flash attention on sm_103a.
+//
+// Computes, per (batch, query head), O = softmax(mask(Q K^T * scale)) V and the
+// natural-log logsumexp LSE_i of each scaled score row, without forming the
+// S x S score matrix ("Phase T14: 融合 Flash-Attention Kernel", section
+// 什么是 flash-attention; "Phase 14: Flash Attention 2 for SM120", section
+// FA2 算法). The online-softmax recurrence keeps a running max m, a running
+// sum l and an accumulator O per query row, rescaling O and l by exp(m_old -
+// m_new) when the max grows; out = O / l and LSE = m + log l at the end.
+//
+// One CTA owns two 128-row query tiles of one (batch, query head) and walks
+// the key/value tiles up to the causal diagonal (tiles wholly above it are
+// never loaded; "Phase 14", section Causal Mask, tile-level skip). Key/value
+// head = query head / (Hq / Hkv) ("Phase 14", section GQA 支持).
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles into two
+//               multi-stage rings (mbarrier full/empty handshakes).
+//   warp 1      tcgen05 MMA issuer (one thread) and TMEM owner:
+//               S_t = Q_t K_j^T (both operands from shared memory) and
+//               O_t += P_t V_j (P_t from tensor memory, V_j from shared memory).
+//   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1: one
+//               thread per query row reads its score row from TMEM, applies
+//               the causal mask inline, does the online-softmax update with
+//               ex2, writes P (bf16/fp16) back to TMEM over its own scores,
+//               rescales O in TMEM when the row max grew by more than 2^8,
+//               and finally writes out = O / l and LSE.
+//
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [384,384+d). P_t is packed two 16-bit values per column into the first
+// 64 columns of S_t, so the next S_t = Q_t K^T may only be issued after the
+// P_t V MMA that reads it has completed (tcgen05 MMAs with different
+// accumulators are not ordered); the issuer waits for that completion.
+//
+// The two softmax groups ping-pong: while one group works on its score tile,
+// the tensor core runs the other tile's P V and Q K^T.
+#include <algorithm>
+#include <type_traits>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kLn2 = 0.6931471805599453f;
+// A row's reference max only moves when the running max exceeds it by more
+// than this many powers of two; until then p = 2^(x - m_ref) <= 2^8, which
+// fp32 accumulation and 16-bit P both hold without loss of range.
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / kChunk;                // 64-col chunks per row
+  static constexpr int kTileBytes = kTileM * D * 2;         // one 128 x D tile
+  static constexpr int kStages = (D == 128) ? 2 : 3;        // K ring and V ring depth
+  static constexpr int kOffQ = 0;                           // 2 Q tiles
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
+  //           s_full[2], p_full[2], pv_done[2], drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+};
+
+struct FwdBars {
+  uint32_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, drain;
+  int stages;
+  __device__ uint32_t kf(int s) const { return k_full + 8 * s; }
+  __device__ uint32_t ke(int s) const { return k_empty + 8 * s; }
+  __device__ uint32_t vf(int s) const { return v_full + 8 * s; }
+  __device__ uint32_t ve(int s) const { return v_empty + 8 * s; }
+  __device__ uint32_t sf(int t) const { return s_full + 8 * t; }
+  __device__ uint32_t pf(int t) const { return p_full + 8 * t; }
+  __device__ uint32_t pv(int t) const { return pv_done + 8 * t; }
+};
+
+// Bounded wait used on the abort path: only the limit can end it.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(status, kStatusWaitTimeout);
+      return;
+    }
+  }
+}
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  constexpr int NS = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+
+  FwdBars bars;
+  bars.stages = NS;
+  bars.q_full = sbase + Cfg::kOffBar;
+  bars.k_full = bars.q_full + 8;
+  bars.k_empty = bars.k_full + 8 * NS;
+  bars.v_full = bars.k_empty + 8 * NS;
+  bars.v_empty = bars.v_full + 8 * NS;
+  bars.s_full = bars.v_empty + 8 * NS;
+  bars.p_full = bars.s_full + 16;
+  bars.pv_done = bars.p_full + 16;
+  bars.drain = bars.pv_done + 16;
+
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+
+  // ---- work assignment: heaviest query-tile pairs first (causal) ----
+  const int BHq = p.B * p.Hq;
+  const int pair = p.n_qpairs - 1 - static_cast<int>(blockIdx.x) / BHq;
+  const int bh = static_cast<int>(blockIdx.x) % BHq;
+  const int b = bh / p.Hq, hq = bh % p.Hq;
+  const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
+  const int n_kv_total = (p.S + kTileN - 1) / kTileN;
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int q0 = pair * 2 * kTileM + t * kTileM;
+    if (q0 >= p.S) n_t[t] = 0;
+    else n_t[t] = p.causal ? min(q0 / kTileN + 1, n_kv_total) : n_kv_total;
+  }
+  const int n_load = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars.q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bars.kf(s), 1);
+      mbar_init(bars.ke(s), 1);
+      mbar_init(bars.vf(s), 1);
+      mbar_init(bars.ve(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.sf(t), 1);
+      mbar_init(bars.pf(t), 4);   // one arrival per softmax warp
+      mbar_init(bars.pv(t), 1);
+    }
+    mbar_init(bars.drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      const uint32_t q_bytes = (n_t[0] > 0 ? Cfg::kTileBytes : 0) + (n_t[1] > 0 ? Cfg::kTileBytes : 0);
+      if (q_bytes) {
+        mbar_arrive_expect_tx(bars.q_full, q_bytes);
+        for (int t = 0; t < 2; ++t) {
+          if (n_t[t] == 0) continue;
+          const int q0 = pair * 2 * kTileM + t * kTileM;
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_3d(sbase + Cfg::kOffQ + t * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_q,
+                        bars.q_full, c * kChunk, q0, bh);
+        }
+      }
+      int j = 0;
+      for (; j < n_load; ++j) {
+        const int st = j % NS;
+        const uint32_t use = static_cast<uint32_t>(j / NS);
+        if (j >= NS && !mbar_wait(bars.ke(st), (use - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(bars.kf(st), Cfg::kTileBytes);
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(sbase + Cfg::kOffK + st * Cfg::kTileBytes + c * (kTileN * 128), &p.tm_k,
+                      bars.kf(st), c * kChunk, j * kTileN, bkv);
+        if (j >= NS && !mbar_wait(bars.ve(st), (use - 1) & 1, abort_flag, p.status)) {
+          ++j;   // the K load of this round is in flight
+          break;
+        }
+        mbar_arrive_expect_tx(bars.vf(st), Cfg::kTileBytes);
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(sbase + Cfg::kOffV + st * Cfg::kTileBytes + c * (kTileN * 128), &p.tm_v,
+                      bars.vf(st), c * kChunk, j * kTileN, bkv);
+      }
+      if (*abort_flag) {
+        // let every copy already issued land before the CTA releases its memory
+        if (q_bytes) drain_wait(bars.q_full, 0, p.status);
+        for (int jj = max(0, j - NS); jj < j; ++jj) {
+          const int st = jj % NS;
+          const uint32_t par = static_cast<uint32_t>(jj / NS) & 1;
+          drain_wait(bars.kf(st), par, p.status);
+          drain_wait(bars.vf(st), par, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    if (lane == 0 && n_load > 0) {
+      constexpr uint32_t idesc_qk = make_idesc(128, kTileN, kBf16, false, false);
+      constexpr uint32_t idesc_pv = make_idesc(128, D, kBf16, false, true);
+      bool ok = mbar_wait(bars.q_full, 0, abort_flag, p.status);
+
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t qa = sbase + Cfg::kOffQ + t * Cfg::kTileBytes;
+        const uint32_t kb = sbase + Cfg::kOffK + st * Cfg::kTileBytes;
+        const uint32_t d_tmem = tmem + t * 128;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
+          mma_ss(d_tmem, make_sdesc(qa + off, 16, 1024), make_sdesc(kb + off, 16, 1024),
+                 idesc_qk, ks > 0);
+        }
+        tc_commit(bars.sf(t));
+      };
+      auto issue_pv = [&](int t, int st, bool accumulate) {
+        const uint32_t vb = sbase + Cfg::kOffV + st * Cfg::kTileBytes;
+        const uint32_t p_tmem = tmem + t * 128;
+        const uint32_t o_tmem = tmem + 256 + t * 128;
+#pragma unroll
+        for (int ks = 0; ks < kTileN / 16; ++ks)
+          mma_ts(o_tmem, p_tmem + ks * 8, make_sdesc(vb + ks * 2048, kTileN * 128, 1024), idesc_pv,
+                 (accumulate || ks > 0) ? 1u : 0u);
+        tc_commit(bars.pv(t));
+      };
+
+      if (ok) ok = mbar_wait(bars.kf(0), 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) issue_qk(t, 0);
+        tc_commit(bars.ke(0));
+      }
+      for (int j = 0; ok && j < n_load; ++j) {
+        const int st = j % NS;
+        const uint32_t par = static_cast<uint32_t>(j / NS) & 1;
+        if (!(ok = mbar_wait(bars.vf(st), par, abort_flag, p.status))) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          if (!(ok = mbar_wait(bars.pf(t), j & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_pv(t, st, j > 0);
+          if (j + 1 < n_t[t]) {
+            const int st1 = (j + 1) % NS;
+            const uint32_t par1 = static_cast<uint32_t>((j + 1) / NS) & 1;
+            if (!(ok = mbar_wait(bars.kf(st1), par1, abort_flag, p.status))) break;
+            // P_t(j) lives in S_t's columns: wait until P_t(j) V_j has read it.
+            if (!(ok = mbar_wait(bars.pv(t), j & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_qk(t, st1);
+          }
+        }
+        if (!ok) break;
+        tc_commit(bars.ve(st));
+        if (j + 1 < n_load) tc_commit(bars.ke((j + 1) % NS));
+      }
+      if (!ok) {
+        // every MMA issued so far must finish before the TMEM is released
+        tc_commit(bars.drain);
+        drain_wait(bars.drain, 0, p.status);
+      }
+    }
+  } else {
+    // ===================== softmax / correction / epilogue =====================
+    const int t = (warp - 2) / 4;               // query tile of this warp group
+    const int quarter = warp & 3;               // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;          // row within the tile
+    const int q0 = pair * 2 * kTileM + t * kTileM;
+    const int row = q0 + r;
+    const int n = n_t[t];
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + t * 128;
+    const uint32_t o_tmem = tmem + lane_off + 256 + t * 128;
+    const float c = p.scale_log2;
+
+    float m_ref = -INFINITY;   // reference max, scaled log2 domain
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bars.sf(t), j & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      float s[kTileN];
+      {
+        uint32_t raw[32];
+#pragma unroll
+        for (int cc = 0; cc < kTileN / 32; ++cc) {
+          tmem_ld32(s_tmem + cc * 32, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(raw[i]);
+        }
+      }
+      const int kv0 = j * kTileN;
+      // inline mask: causal (key > query) and keys past the sequence end
+      const int lim = p.causal ? min(row, p.S - 1) : p.S - 1;   // last visible key
+      if (kv0 + kTileN - 1 > lim) {
+#pragma unroll
+        for (int i = 0; i < kTileN; ++i)
+          if (kv0 + i > lim) s[i] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int i = 4; i < kTileN; i += 4) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+        mx2 = fmaxf(mx2, s[i + 2]);
+        mx3 = fmaxf(mx3, s[i + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      float m_new = m_ref;
+      if (mx > m_ref + kRescaleThreshold) m_new = mx;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2(m_ref - m_use);   // 0 when m_ref = -inf
+      const bool moved = (m_new != m_ref);
+      m_ref = m_new;
+
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[h * 64 + 2 * i], c, -m_use));
+          const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], c, -m_use));
+          sum0 += p0;
+          sum1 += p1;
+          pk[i] = pack2<kBf16>(p0, p1);
+        }
+        tmem_st32(s_tmem + h * 32, pk);
+      }
+      l = l * alpha + (sum0 + sum1);
+
+      // O <- alpha * O for rows whose reference max moved (not needed for the
+      // first tile: its P V overwrites O)
+      if (j > 0 && __any_sync(0xffffffffu, moved)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (j - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        const float a = moved ? alpha : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_tmem + cc * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+          tmem_st32(o_tmem + cc * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.pf(t));
+    }
+
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (n - 1) & 1, abort_flag, p.status));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
+        Elem* orow = reinterpret_cast<Elem*>(p.out) + (static_cast<size_t>(bh) * p.S + row) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_tmem + cc * 32, o);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
+                                __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (row < p.S) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+        if (row < p.S)
+          p.lse[static_cast<size_t>(bh) * p.S + row] = (m_ref + __log2f(l)) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
+  constexpr int smem = FwdCfg<D>::kSmemBytes;
+  auto kernel = fa_fwd_kernel<D, kBf16>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.B * p.Hq * p.n_qpairs);
+  kernel<<<grid, kFwdThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdParams& p, int d, bool bf16, cudaStream_t stream) {
+  if (d == 128) return bf16 ? launch_fwd_impl<128, true>(p, stream) : launch_fwd_impl<128, false>(p, stream);
+  return bf16 ? launch_fwd_impl<64, true>(p, stream) : launch_fwd_impl<64, false>(p, stream);
+}
+
+}  // namespace fa

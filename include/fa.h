@@ -1,0 +1,124 @@
+/*
+ * fa.h — C ABI of libfa: causal scaled-dot-product flash attention, forward
+ * and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed. For every batch b and query head h (key/value head
+ * g = h / (Hq / Hkv), grouped-query attention as in "Phase 14: Flash
+ * Attention 2 for SM120", section GQA 支持):
+ *
+ *   s_ij   = scale * <Q[b,h,i,:], K[b,g,j,:]>,  s_ij = -inf for j > i if causal
+ *   P_ij   = exp(s_ij - LSE_i),   LSE_i = log(sum_j exp(s_ij))   (natural log)
+ *   out_i  = sum_j P_ij V[b,g,j,:]
+ *
+ * ("Phase T14: 融合 Flash-Attention Kernel", section 什么是 flash-attention,
+ * and its Key Design Decisions item 2: the forward keeps only LSE per row).
+ * The backward recomputes P from Q, K, V and LSE, forms D_i = <dO_i, out_i>
+ * (item 3 of the same section) and
+ *
+ *   dP_ij = <dO_i, V_j>,  dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij K_j,  dK_j = scale * sum_i dS_ij Q_i,
+ *   dV_j  = sum_i P_ij dO_i
+ *
+ * with dK, dV of a key/value head summed over its Hq/Hkv query heads. No S x S
+ * matrix is ever stored.
+ *
+ * Layout. Every tensor is a dense, contiguous array in device memory:
+ *   q, out, dout, dq : [B][Hq][S][d]      k, v, dk, dv : [B][Hkv][S][d]
+ *   lse              : [B][Hq][S]  float32
+ * Element type of q/k/v/out/dout/dq/dk/dv is `dtype` (FA_F32, FA_F16 or
+ * FA_BF16). d must be 64 or 128. Every pointer must be 16-byte aligned.
+ *
+ * Precision. FA_BF16 / FA_F16 run on the tensor cores with fp32 accumulation;
+ * P is rounded to the input type before it multiplies V (and dS before it
+ * multiplies Q and K). FA_F32 runs on plain fp32 arithmetic.
+ *
+ * Ownership and execution. The caller owns every buffer; the library keeps no
+ * pointer after a call returns and allocates no device memory. Calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ * run on the current CUDA device, which must be the stream's device. Outputs
+ * are overwritten, never accumulated into. Calls that share output or
+ * workspace buffers must be ordered by the caller.
+ *
+ * Errors. Functions return FA_OK (0) or a negative FA_ERR_* code. Argument
+ * errors are detected on the host before anything is enqueued, so a call that
+ * returns an argument error has written nothing. FA_ERR_CUDA means a CUDA
+ * runtime call or a kernel launch failed (the CUDA error is left for
+ * cudaGetLastError to report). A kernel that gives up an internal wait (it
+ * never should) sets a device status word instead of hanging; read it with
+ * fa_last_device_status.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+enum {
+  FA_OK = 0,
+  FA_ERR_SHAPE = -1,        /* B, Hq, Hkv, S < 1, Hq % Hkv != 0, d not 64/128, or too large */
+  FA_ERR_DTYPE = -2,        /* dtype not one of fa_dtype */
+  FA_ERR_NULL = -3,         /* a required pointer is NULL */
+  FA_ERR_ALIGN = -4,        /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = -5,    /* workspace NULL or smaller than fa_bwd_workspace_bytes */
+  FA_ERR_CUDA = -6,         /* a CUDA runtime call or kernel launch failed */
+  FA_ERR_SCALE = -7,        /* scale not finite and > 0 */
+  FA_ERR_TMA = -8           /* the driver rejected a tensor-memory-access descriptor */
+};
+
+/*
+ * Forward pass. Writes out[B][Hq][S][d] (dtype) and lse[B][Hq][S] (float32,
+ * natural-log logsumexp of the scaled, masked score row). causal != 0 masks
+ * key positions j > i. scale is usually 1/sqrt(d).
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+           int B, int Hq, int Hkv, int S, int d, int causal, float scale,
+           int dtype, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes (the same for every
+ * dtype): an fp32 dQ accumulator [B][Hq][S128][d], D and LSE*log2(e) rows
+ * [B][Hq][S128] each, where S128 = S rounded up to a multiple of 128, each
+ * region starting on a 256-byte boundary. Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int S, int d);
+
+/*
+ * Backward pass. Inputs: q, k, v, out and lse from fa_fwd with the same
+ * arguments, dout = dL/dout. Writes dq [B][Hq][S][d], dk and dv [B][Hkv][S][d]
+ * (dtype). `workspace` is caller-owned device memory of at least
+ * fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) bytes, 256-byte aligned; its
+ * contents on entry do not matter and are clobbered.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* out,
+           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+           int B, int Hq, int Hkv, int S, int d, int causal, float scale,
+           int dtype, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream);
+
+/* Static description of an FA_* code. */
+const char* fa_strerror(int code);
+
+/*
+ * Waits for `stream`, then reads and clears the device status word of the
+ * current device: 0 when no kernel has given up a wait since the last read,
+ * else a bit mask (1 = an mbarrier wait ran past its limit). Returns FA_OK or
+ * FA_ERR_CUDA.
+ */
+int fa_last_device_status(fa_stream_t stream, int* status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -10,3 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session")
+def fa_lib():
+    """Build libfa.so in-tree (if stale) and return the binding module."""
+    from causal_flash_attention_gb300 import build as fa_build
+    fa_build.build()
+    import causal_flash_attention_gb300 as fa
+    fa.lib()
+    return fa

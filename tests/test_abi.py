@@ -1,0 +1,110 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/fa.h declares, and rejects bad arguments on the host with the
+documented codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+FA_OK, FA_ERR_SHAPE, FA_ERR_DTYPE, FA_ERR_NULL, FA_ERR_ALIGN, FA_ERR_WORKSPACE, \
+    FA_ERR_CUDA, FA_ERR_SCALE, FA_ERR_TMA = 0, -1, -2, -3, -4, -5, -6, -7, -8
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_strerror",
+              "fa_last_device_status", "fa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fa_lib):
+    L = fa_lib.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), f"libfa.so does not export {n}"
+
+
+def test_error_codes_match_header():
+    text = open(HEADER).read()
+    for name, val in [("FA_OK", 0), ("FA_ERR_SHAPE", -1), ("FA_ERR_DTYPE", -2),
+                      ("FA_ERR_NULL", -3), ("FA_ERR_ALIGN", -4), ("FA_ERR_WORKSPACE", -5),
+                      ("FA_ERR_CUDA", -6), ("FA_ERR_SCALE", -7), ("FA_ERR_TMA", -8)]:
+        assert re.search(rf"\b{name}\s*=\s*{val}\b", text), name
+
+
+def test_strerror_and_version(fa_lib):
+    for code in range(0, -9, -1):
+        s = fa_lib.fa_strerror(code)
+        assert s and s != "unknown error code"
+    assert fa_lib.fa_strerror(-99) == "unknown error code"
+    assert fa_lib.fa_version() >= 10000
+
+
+def _fwd(L, q=16, k=16, v=16, out=16, lse=16, B=1, Hq=2, Hkv=1, S=128, d=64, causal=1,
+         scale=0.125, dtype=2):
+    return L.fa_fwd(q, k, v, out, lse, B, Hq, Hkv, S, d, causal, scale, dtype, None)
+
+
+def _bwd(L, ptr=256, B=1, Hq=2, Hkv=1, S=128, d=64, scale=0.125, dtype=2, ws=256,
+         ws_bytes=1 << 30, **over):
+    ptrs = dict(q=ptr, k=ptr, v=ptr, out=ptr, dout=ptr, lse=ptr, dq=ptr, dk=ptr, dv=ptr)
+    ptrs.update(over)
+    return L.fa_bwd(ptrs["q"], ptrs["k"], ptrs["v"], ptrs["out"], ptrs["dout"], ptrs["lse"],
+                    ptrs["dq"], ptrs["dk"], ptrs["dv"], B, Hq, Hkv, S, d, 1, scale, dtype,
+                    ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=32), FA_ERR_SHAPE), (dict(d=96), FA_ERR_SHAPE), (dict(d=256), FA_ERR_SHAPE),
+    (dict(S=0), FA_ERR_SHAPE), (dict(B=0), FA_ERR_SHAPE), (dict(Hq=3, Hkv=2), FA_ERR_SHAPE),
+    (dict(Hkv=0), FA_ERR_SHAPE), (dict(dtype=3), FA_ERR_DTYPE), (dict(dtype=-1), FA_ERR_DTYPE),
+    (dict(scale=0.0), FA_ERR_SCALE), (dict(scale=-1.0), FA_ERR_SCALE),
+    (dict(scale=float("nan")), FA_ERR_SCALE), (dict(scale=float("inf")), FA_ERR_SCALE),
+    (dict(q=None), FA_ERR_NULL), (dict(lse=None), FA_ERR_NULL), (dict(out=None), FA_ERR_NULL),
+    (dict(q=8), FA_ERR_ALIGN), (dict(v=24), FA_ERR_ALIGN), (dict(lse=4), FA_ERR_ALIGN),
+])
+def test_fwd_rejects_bad_arguments(fa_lib, kw, code):
+    assert _fwd(fa_lib.lib(), **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=48), FA_ERR_SHAPE), (dict(Hq=5, Hkv=2), FA_ERR_SHAPE), (dict(dtype=7), FA_ERR_DTYPE),
+    (dict(dq=None), FA_ERR_NULL), (dict(dout=None), FA_ERR_NULL), (dict(dv=8), FA_ERR_ALIGN),
+    (dict(ws=None), FA_ERR_WORKSPACE), (dict(ws_bytes=1024), FA_ERR_WORKSPACE),
+    (dict(ws=16 + 256), FA_ERR_ALIGN), (dict(scale=0.0), FA_ERR_SCALE),
+])
+def test_bwd_rejects_bad_arguments(fa_lib, kw, code):
+    assert _bwd(fa_lib.lib(), **kw) == code
+
+
+def test_workspace_size_formula(fa_lib):
+    def expect(B, Hq, S, d):
+        up = lambda x, m: (x + m - 1) // m * m
+        bh, sp = B * Hq, up(S, 128)
+        return up(bh * sp * d * 4, 256) + 2 * up(bh * sp * 4, 256)
+    for B, Hq, Hkv, S, d in [(1, 2, 2, 128, 64), (8, 12, 12, 1024, 64), (4, 32, 8, 2048, 128),
+                             (1, 32, 32, 8192, 128), (1, 1, 1, 1, 64), (3, 4, 2, 200, 128)]:
+        assert fa_lib.fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) == expect(B, Hq, S, d)
+    assert fa_lib.fa_bwd_workspace_bytes(1, 3, 2, 128, 64) == 0
+    assert fa_lib.fa_bwd_workspace_bytes(1, 1, 1, 128, 80) == 0
+
+
+def test_status_requires_output_pointer(fa_lib):
+    assert fa_lib.lib().fa_last_device_status(None, None) == FA_ERR_NULL
+
+
+def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
+    import causal_flash_attention_gb300 as fa
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        fa.lib()
