@@ -1,0 +1,417 @@
+"""Benchmark: causal flash attention forward + backward on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole path over one batch: fa_fwd (out, lse) then
+fa_bwd (dq, dk, dv) through the C ABI on the long_8k workload (bf16, B=1,
+Hq=Hkv=32, S=8192, d=128, causal, synthetic seeded inputs with spike keys).
+FLOPs follow the causal convention 2*B*Hq*S^2*d (forward) + 5*B*Hq*S^2*d
+(backward). Each rank runs its own replica (no collective on the data path);
+`value` is the FLOPs of all ranks divided by the slowest rank's time.
+
+Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle
+instead (the reference arm), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fa_inputs  # noqa: E402
+
+METRIC = "causal attention fwd/bwd TFLOP/s and % of GB300 dense BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------ arithmetic --
+def flops(w, fwd=True, bwd=True):
+    """Causal FLOP convention: forward 2*B*Hq*S^2*d, backward 5*B*Hq*S^2*d."""
+    base = w.B * w.Hq * w.S * w.S * w.d
+    return (2 * base if fwd else 0) + (5 * base if bwd else 0)
+
+
+def elem_bytes(w):
+    return {"fp32": 4, "fp16": 2, "bf16": 2}[w.dtype]
+
+
+def tensor_bytes(B, H, S, d, esize):
+    return B * H * S * d * esize
+
+
+def score_matrix_bytes(B, H, S, esize):
+    """Bytes of one materialised [B, H, S, S] score (or probability) matrix,
+    the tensor flash attention never stores."""
+    return B * H * S * S * esize
+
+
+def fwd_algorithmic_bytes(w):
+    """Compulsory HBM traffic of one forward: read Q, K, V, write O and LSE."""
+    e = elem_bytes(w)
+    return (2 * tensor_bytes(w.B, w.Hq, w.S, w.d, e) + 2 * tensor_bytes(w.B, w.Hkv, w.S, w.d, e)
+            + w.B * w.Hq * w.S * 4)
+
+
+def bwd_algorithmic_bytes(w):
+    """Compulsory HBM traffic of one backward: read Q, K, V, O, dO, LSE, write
+    dQ, dK, dV."""
+    e = elem_bytes(w)
+    q = tensor_bytes(w.B, w.Hq, w.S, w.d, e)
+    kv = tensor_bytes(w.B, w.Hkv, w.S, w.d, e)
+    return 4 * q + 4 * kv + w.B * w.Hq * w.S * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "causal_flash_attention_gb300", "csrc")
+    for name in ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch recorded from an ncu capture in
+    profiles/dram_traffic.txt, valid only while the kernel sources hash the
+    same as when it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and \
+                parts[1] == workload and parts[2] == want:
+            return float(parts[3])
+    return None
+
+
+# --------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        under_load = [x for x in sm if x > 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(under_load), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [i["num_threads"] for i in info if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n)), "BLAS threads (threadpoolctl)"
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0)), "cores available (BLAS default)"
+    except AttributeError:
+        return os.cpu_count() or 1, "cores available (BLAS default)"
+
+
+def oracle_inputs(w, heads):
+    """float64 copies of batch 0, query heads [0, heads) and their key/value heads."""
+    import torch
+    q, k, v, do = fa_inputs.make_inputs(w)
+    G = w.Hq // w.Hkv
+    f64 = lambda t: t.to(torch.float64).numpy()
+    return [(f64(q[:1, h:h + 1]), f64(k[:1, h // G:h // G + 1]), f64(v[:1, h // G:h // G + 1]),
+             f64(do[:1, h:h + 1])) for h in range(heads)]
+
+
+def oracle_sample(w, head_inputs, rows):
+    """Time the fp64 oracle's dense forward + backward on the causal leading
+    block (query rows and keys 0..rows-1) of one head of workload `w`. Under the
+    causal mask those rows see only those keys, so this is an exact piece of the
+    full problem. Returns (seconds, causal-convention flops 7*rows^2*d)."""
+    import oracle
+    Q, K, V, DO = (x[:, :, :rows] for x in head_inputs)
+    t0 = time.perf_counter()
+    oracle.forward(Q, K, V, w.causal, w.scale)
+    oracle.backward(Q, K, V, DO, w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    return dt, 7 * rows * rows * w.d
+
+
+# ---------------------------------------------------------------- GPU arm --
+def run_gpu(args, w, rank, world, local_rank):
+    import torch
+    import causal_flash_attention_gb300 as fa
+
+    fa.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    q, k, v, do = fa_inputs.make_inputs(w)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    out = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = fa.workspace_for(qd, kd)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale, stream)
+        fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    status = fa.fa_last_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        for s in range(K):
+            ev[s][0].record(stream)
+            fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale, stream)
+            ev[s][1].record(stream)
+            fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
+            ev[s][2].record(stream)
+        barrier()
+        total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+        fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+        # end to end: pinned host inputs -> device, fwd + bwd, results -> pinned host
+        hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, do))
+        h_out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        h_lse = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+        h_dq = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        h_dk = torch.empty(k.shape, dtype=k.dtype).pin_memory()
+        h_dv = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in (h_out, h_lse, h_dq, h_dk, h_dv))
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            dod.copy_(hdo, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            h_dq.copy_(dq, non_blocking=True)
+            h_dk.copy_(dk, non_blocking=True)
+            h_dv.copy_(dv, non_blocking=True)
+
+        K2 = max(3, K // 4)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / K2
+    status = fa.fa_last_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    t = torch.tensor([total_ms, fwd_ms, bwd_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, fwd_ms, bwd_ms, e2e_ms = t.tolist()
+    return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms,
+                h2d=h2d, d2h=d2h, clocks=clocks.summary(), dist=dist)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="long_8k", choices=sorted(fa_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    w = fa_inputs.WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    step_flops = flops(w, True, w.backward)
+    l2_note = (f"inputs larger than L2: Q,K,V,dO = "
+               f"{(fwd_algorithmic_bytes(w) + tensor_bytes(w.B, w.Hq, w.S, w.d, elem_bytes(w))) / 2**20:.0f} MiB "
+               f"read per step vs {L2_BYTES / 2**20:.0f} MiB L2; no flush")
+    config = {"workload": w.describe(), "global_batch": w.B * world, "seq_len": w.S,
+              "heads": [w.Hq, w.Hkv], "head_dim": w.d, "causal": w.causal,
+              "parallelism": f"replicas x{world}", "l2": l2_note}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cores, how = cpu_threads()
+        rows = min(w.S, 2048)
+        inputs = oracle_inputs(w, min(w.Hq, 4))
+        times = []
+        for i in range(args.warmup + args.steps):
+            dt, fl = oracle_sample(w, inputs[i % len(inputs)], rows)
+            if i >= args.warmup:
+                times.append(dt)
+        sec = statistics.mean(times)
+        value = fl / sec / 1e12
+        sample = (f"per step: fp64 dense forward + softmax-Jacobian backward of the causal "
+                  f"leading {rows}x{rows} block (rows and keys 0..{rows - 1}) of one query "
+                  f"head of {w.name}, heads 0..{len(inputs) - 1} in turn; {fl / 1e9:.2f} GFLOP "
+                  f"by the causal convention")
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                                 "cores_source": how, "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line))
+        return
+
+    r = run_gpu(args, w, rank, world, local_rank)
+    if rank != 0:
+        if r["dist"] is not None:
+            r["dist"].destroy_process_group()
+        return
+    K = args.steps
+    ms_per_step = r["total_ms"] / K
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    fwd_tf = flops(w, True, False) / (r["fwd_ms"] * 1e-3) / 1e12
+    bwd_tf = flops(w, False, True) / (r["bwd_ms"] * 1e-3) / 1e12 if w.backward else None
+    e2e_tf = step_flops * world / (r["e2e_ms"] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = recorded_traffic("fa_bwd_kernel", w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else w.dtype,
+        "data": "synthetic (seeded N(0,1)-based inputs, no dataset)", "config": config,
+        "pct_of_peak": {"step": 100 * value / world / peak, "fwd": 100 * fwd_tf / peak,
+                        "bwd": (100 * bwd_tf / peak) if bwd_tf else None,
+                        "peak_tflops": peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                        "step_vs_sustained": 100 * value / world / peaks["bf16_tflops_sustained"]},
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
+        "roofline": {
+            "kernel": "fa_bwd_kernel (timed as the fa_bwd call: D pre-pass + main kernel + dQ convert)",
+            "bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
+            "frac": (bwd_tf / peak) if bwd_tf else None, "traffic": traffic,
+            "traffic_unit": "bytes per launch (dram read + write)",
+            "algorithmic_bytes": bwd_algorithmic_bytes(w),
+            "peak_source": f"{peak_src} bf16_tflops (burst)",
+        },
+        "roofline_fwd": {
+            "kernel": "fa_fwd_kernel (one launch per fa_fwd call)", "bound": "tensor",
+            "achieved": fwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
+            "algorithmic_bytes": fwd_algorithmic_bytes(w),
+        },
+        "e2e": {"value": e2e_tf, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+        "gpu_launches": (1 + 3) * K,
+        "clocks": r["clocks"],
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cores, how = cpu_threads()
+        total_t, total_f = 0.0, 0
+        for hin in oracle_inputs(w, 2):
+            dt, fl = oracle_sample(w, hin, w.S)
+            total_t += dt
+            total_f += fl
+        line["cpu_baseline"] = {
+            "value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "cores_source": how, "kind": "oracle",
+            "sample": f"fp64 dense forward + softmax-Jacobian backward of query heads 0 and 1 "
+                      f"(all {w.S} rows and keys) of {w.name}: {total_f / 1e9:.1f} GFLOP by "
+                      f"the causal convention in {total_t:.2f} s"}
+    if r["dist"] is not None:
+        r["dist"].destroy_process_group()
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
