@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_strerror",
     "fa_last_device_status", "fa_version", "attention_forward", "attention_backward",
-    "DTYPE_CODES",
+    "DTYPE_CODES", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
@@ -157,3 +157,26 @@ def attention_backward(q, k, v, out, dout, lse, causal=True, scale=None, workspa
         workspace = workspace_for(q, k)
     fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
     return dq, dk, dv
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
+
+
+def fa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, causal=True, scale=None, stream=None):
+    """Call fa_bwd_noalloc: fa_bwd without a workspace, for callers that cannot
+    allocate device memory; the scratch is a fixed array inside libfa (see
+    include/fa.h for its size, sharing and ordering rules)."""
+    L = lib()
+    fn = L.fa_bwd_noalloc
+    if fn.argtypes is None:
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp]
+        fn.restype = i32
+    _check_contig(q, k, v, out, dout, lse, dq, dk, dv)
+    B, Hq, Hkv, S, d = _dims(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
+            _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_bwd_noalloc")

@@ -110,6 +110,8 @@ const char* fa_strerror(int code) {
     case FA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case FA_ERR_SCALE: return "scale must be finite and > 0";
     case FA_ERR_TMA: return "the driver rejected a tensor-memory-access descriptor";
+    case FA_ERR_NOALLOC_LIMIT:
+      return "sizes need more scratch than fa_bwd_noalloc's fixed FA_NOALLOC_SCRATCH_BYTES";
     default: return "unknown error code";
   }
 }

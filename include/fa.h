@@ -70,7 +70,8 @@ enum {
   FA_ERR_WORKSPACE = -5,    /* workspace NULL or smaller than fa_bwd_workspace_bytes */
   FA_ERR_CUDA = -6,         /* a CUDA runtime call or kernel launch failed */
   FA_ERR_SCALE = -7,        /* scale not finite and > 0 */
-  FA_ERR_TMA = -8           /* the driver rejected a tensor-memory-access descriptor */
+  FA_ERR_TMA = -8,          /* the driver rejected a tensor-memory-access descriptor */
+  FA_ERR_NOALLOC_LIMIT = -9 /* fa_bwd_noalloc: sizes need more than FA_NOALLOC_SCRATCH_BYTES */
 };
 
 /*
@@ -102,6 +103,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out,
            int B, int Hq, int Hkv, int S, int d, int causal, float scale,
            int dtype, void* workspace, size_t workspace_bytes,
            fa_stream_t stream);
+
+/*
+ * Size of the fixed device scratch array behind fa_bwd_noalloc (32 MiB). A
+ * call fits when fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) is at most this,
+ * e.g. B*Hq = 96 heads at S = 1024, d = 64 (about 25.9 MB).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * Backward pass for callers that cannot allocate device memory (for example
+ * code inside a framework or plugin callback that owns every device
+ * allocation, or latency-critical code that must not call cudaMalloc/cudaFree
+ * because they can synchronize the device). Same arguments, results and
+ * errors as fa_bwd, without the workspace: the scratch is a fixed
+ * FA_NOALLOC_SCRATCH_BYTES array in the library's device memory, held on every
+ * GPU that loads the library until the process exits. The call allocates
+ * nothing. This entry point has no counterpart in the method's description;
+ * it is a deployment aid.
+ *
+ * Limits and sharing: returns FA_ERR_NOALLOC_LIMIT, having enqueued nothing,
+ * when the sizes need more scratch than FA_NOALLOC_SCRATCH_BYTES. The first
+ * call made with a given device current looks up the array's device address
+ * on that device; make that first call before any stream capture. Every call
+ * shares the one array and it keeps the last call's contents (each call
+ * rewrites all of it that it reads, so results do not depend on them). Calls
+ * whose work overlaps on the GPU (unordered streams, concurrent host threads)
+ * race on the array: the caller must order them.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                   const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                   int B, int Hq, int Hkv, int S, int d, int causal, float scale,
+                   int dtype, fa_stream_t stream);
 
 /* Static description of an FA_* code. */
 const char* fa_strerror(int code);
