@@ -276,8 +276,8 @@ def run_gpu(args, w, rank, world, local_rank):
             h_dk.copy_(dk, non_blocking=True)
             h_dv.copy_(dv, non_blocking=True)
 
-        K2 = max(3, K // 4)
-        for _ in range(2):
+        K2 = 0 if args.no_e2e else max(3, K // 4)
+        for _ in range(2 if K2 else 0):
             e2e_step()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -286,7 +286,7 @@ def run_gpu(args, w, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         barrier()
-        e2e_ms = e0.elapsed_time(e1) / K2
+        e2e_ms = e0.elapsed_time(e1) / K2 if K2 else float("nan")
     status = fa.fa_last_device_status(stream)
     if status:
         raise RuntimeError(f"device status {status} in the timed region")
@@ -307,6 +307,10 @@ def main():
     ap.add_argument("--workload", default="long_8k", choices=sorted(fa_inputs.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer timing")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override Hq (and Hkv in the same ratio): a smaller case of the same "
+                         "workload, e.g. for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -315,6 +319,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     w = fa_inputs.WORKLOADS[args.workload]
+    if args.heads:
+        import dataclasses
+        G = w.Hq // w.Hkv
+        if args.heads % G:
+            ap.error(f"--heads must be a multiple of {G}")
+        w = dataclasses.replace(w, Hq=args.heads, Hkv=args.heads // G)
     peaks, peak_src = load_peaks()
     step_flops = flops(w, True, w.backward)
     l2_note = (f"inputs larger than L2: Q,K,V,dO = "
@@ -363,7 +373,8 @@ def main():
     value = step_flops * world / (ms_per_step * 1e-3) / 1e12
     fwd_tf = flops(w, True, False) / (r["fwd_ms"] * 1e-3) / 1e12
     bwd_tf = flops(w, False, True) / (r["bwd_ms"] * 1e-3) / 1e12 if w.backward else None
-    e2e_tf = step_flops * world / (r["e2e_ms"] * 1e-3) / 1e12
+    e2e_tf = (step_flops * world / (r["e2e_ms"] * 1e-3) / 1e12) if r["e2e_ms"] == r["e2e_ms"] \
+        else None
     peak = peaks["bf16_tflops"]
     traffic = recorded_traffic("fa_bwd_kernel", w.name)
     line = {

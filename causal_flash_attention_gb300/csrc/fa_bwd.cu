@@ -141,6 +141,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using Cfg = BwdCfg<D>;
   constexpr int NS = Cfg::kStages;
+  // d = 128: dQ is formed transposed, dQ^T = K_j^T dS^T (TMEM lanes = head
+  // dimension), so each warp's reduction into the accumulator covers one
+  // contiguous 128-byte row segment. For d = 64 that would be an M = 64 MMA,
+  // so there dQ = dS K_j (TMEM lanes = query rows) and each thread adds its
+  // row with 16-byte vector reductions.
+  constexpr bool kDqT = (D == 128);
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {   // the 128-byte swizzle needs 1024-byte aligned tiles
@@ -249,64 +255,95 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ===================== MMA issuer =====================
+    // Issue order per step n (S^T(n+1) goes ahead of dQ(n) so the softmax warps
+    // compute P(n+1) while the tensor core finishes step n):
+    //   dV(n) [P(n) ready]  dK(n) [dS(n) ready]  S^T(n+1) [dV(n) done: P(n) read]
+    //   dQ(n)  dP^T(n+1) [dQ(n) read out of TMEM]
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kTileM, kBf16, false, false);  // S^T, dP^T
       constexpr uint32_t idesc_kv = make_idesc(128, D, kBf16, false, true);       // dV, dK
-      constexpr uint32_t idesc_q = make_idesc(128, D, kBf16, true, true);         // dQ
+      constexpr uint32_t idesc_q = kDqT ? make_idesc(128, kTileM, kBf16, true, true)
+                                        : make_idesc(128, D, kBf16, true, true);  // dQ^T / dQ
       const uint32_t t_dk = tmem, t_dv = tmem + 128, t_s = tmem + 256, t_dp = tmem + 384;
       const uint32_t k_s = sbase + Cfg::kOffK, v_s = sbase + Cfg::kOffV;
       const uint32_t ds_s = sbase + Cfg::kOffDS;
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status);
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int st = it % NS;
-        const uint32_t par = static_cast<uint32_t>(it / NS) & 1;
-        const uint32_t q_s = sbase + Cfg::kOffQ + st * Cfg::kTileBytes;
-        const uint32_t do_s = sbase + Cfg::kOffDO + st * Cfg::kTileBytes;
-        if (!(ok = mbar_wait(qdo_full(st), par, abort_flag, p.status))) break;
-        if (it > 0 && !(ok = mbar_wait(dv_done, (it - 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // S^T = K_j Q_i^T
+      auto q_s = [&](int st) { return sbase + Cfg::kOffQ + st * Cfg::kTileBytes; };
+      auto do_s = [&](int st) { return sbase + Cfg::kOffDO + st * Cfg::kTileBytes; };
+
+      auto issue_s = [&](int st) {   // S^T = K_j Q_i^T
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
-          mma_ss(t_s, make_sdesc(k_s + off, 16, 1024), make_sdesc(q_s + off, 16, 1024), idesc_s,
-                 ks > 0);
+          mma_ss(t_s, make_sdesc(k_s + off, 16, 1024), make_sdesc(q_s(st) + off, 16, 1024),
+                 idesc_s, ks > 0);
         }
         tc_commit(s_full);
-        if (it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // dP^T = V_j dO_i^T
+      };
+      auto issue_dp = [&](int st) {   // dP^T = V_j dO_i^T
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
-          mma_ss(t_dp, make_sdesc(v_s + off, 16, 1024), make_sdesc(do_s + off, 16, 1024), idesc_s,
-                 ks > 0);
+          mma_ss(t_dp, make_sdesc(v_s + off, 16, 1024), make_sdesc(do_s(st) + off, 16, 1024),
+                 idesc_s, ks > 0);
         }
         tc_commit(dp_full);
-        if (!(ok = mbar_wait(p_full, it & 1, abort_flag, p.status))) break;
+      };
+
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status) &&
+                mbar_wait(qdo_full(0), 0, abort_flag, p.status);
+      if (ok) {
         tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int n = 0; ok && n < n_iter; ++n) {
+        const int st = n % NS;
+        const int st1 = (n + 1) % NS;
+        const bool more = n + 1 < n_iter;
         // dV += P^T dO_i  (P^T from TMEM, 16-bit packed in S^T's first 64 columns)
+        if (!(ok = mbar_wait(p_full, n & 1, abort_flag, p.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTileM / 16; ++ks)
-          mma_ts(t_dv, t_s + ks * 8, make_sdesc(do_s + ks * 2048, kTileM * 128, 1024), idesc_kv,
-                 (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(t_dv, t_s + ks * 8, make_sdesc(do_s(st) + ks * 2048, kTileM * 128, 1024),
+                 idesc_kv, (n > 0 || ks > 0) ? 1u : 0u);
         tc_commit(dv_done);
-        if (!(ok = mbar_wait(ds_full, it & 1, abort_flag, p.status))) break;
-        tc_fence_after();
         // dK += dS^T Q_i
+        if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, p.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTileM / 16; ++ks)
           mma_ss(t_dk, make_sdesc(ds_s + (ks / 4) * (kTileN * 128) + (ks % 4) * 32, 16, 1024),
-                 make_sdesc(q_s + ks * 2048, kTileM * 128, 1024), idesc_kv,
-                 (it > 0 || ks > 0) ? 1u : 0u);
-        // dQ = dS K_j  (dS read MN-major from the same dS^T tile)
+                 make_sdesc(q_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
+                 (n > 0 || ks > 0) ? 1u : 0u);
+        // S^T for the next step, once dV(n) has consumed P^T(n)
+        if (more) {
+          if (!(ok = mbar_wait(qdo_full(st1), static_cast<uint32_t>((n + 1) / NS) & 1,
+                               abort_flag, p.status)))
+            break;
+          if (!(ok = mbar_wait(dv_done, n & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_s(st1);
+        }
+        // dQ (into dP^T's columns: the softmax warps have read dP^T(n))
 #pragma unroll
-        for (int ks = 0; ks < kTileN / 16; ++ks)
-          mma_ss(t_dp, make_sdesc(ds_s + ks * 2048, kTileM * 128, 1024),
-                 make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
+        for (int ks = 0; ks < kTileN / 16; ++ks) {
+          if constexpr (kDqT)   // dQ^T = K_j^T dS^T
+            mma_ss(t_dp, make_sdesc(k_s + ks * 2048, kTileN * 128, 1024),
+                   make_sdesc(ds_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
+          else                  // dQ = dS K_j
+            mma_ss(t_dp, make_sdesc(ds_s + ks * 2048, kTileN * 128, 1024),
+                   make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
+        }
         tc_commit(dq_full);
-        tc_commit(qdo_empty(st));
         tc_commit(ds_empty);
+        tc_commit(qdo_empty(st));
+        // dP^T for the next step, once dQ(n) has left TMEM
+        if (more) {
+          if (!(ok = mbar_wait(dq_empty, n & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_dp(st1);
+        }
       }
       tc_commit(ok ? kd_done : drain);
       if (!ok) drain_wait(drain, 0, p.status);
@@ -338,25 +375,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = i * kTileM;
       uint32_t ppk[64];
 #pragma unroll
-      for (int cc = 0; cc < kTileM / 32; ++cc) {
-        uint32_t raw[32];
-        tmem_ld32(t_s + cc * 32, raw);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t raw[64];
+        tmem_ld32(t_s + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+        tmem_ld32(t_s + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int qc = cc * 32 + e;
+        for (int e = 0; e < 64; e += 2) {
+          const int qc = h * 64 + e;
           float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[qc]));
           float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[qc + 1]));
           if (any_mask) {
             if (kv >= p.S || (p.causal && kv > q0 + qc)) p0 = 0.f;
             if (kv >= p.S || (p.causal && kv > q0 + qc + 1)) p1 = 0.f;
           }
-          ppk[cc * 16 + e / 2] = pack2<kBf16>(p0, p1);
+          ppk[h * 32 + e / 2] = pack2<kBf16>(p0, p1);
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = ppk[cc * 16 + e];
-        tmem_st16(t_s + cc * 16, w);
+        tmem_st32(t_s + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(ppk + h * 32));
       }
       tmem_wait_st();
       tc_fence_before();
@@ -368,27 +403,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < kTileM / 32; ++cc) {
-        uint32_t raw[32];
-        tmem_ld32(t_dp + cc * 32, raw);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t raw[64];
+        tmem_ld32(t_dp + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+        tmem_ld32(t_dp + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
         tmem_wait_ld();
-        uint32_t w[16];
+        uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int qc = cc * 32 + e;
-          const float2 pp = unpack2<kBf16>(ppk[cc * 16 + e / 2]);
+        for (int e = 0; e < 64; e += 2) {
+          const int qc = h * 64 + e;
+          const float2 pp = unpack2<kBf16>(ppk[h * 32 + e / 2]);
           const float d0 = pp.x * (__uint_as_float(raw[e]) - dls[qc]);
           const float d1 = pp.y * (__uint_as_float(raw[e + 1]) - dls[qc + 1]);
           w[e / 2] = pack2<kBf16>(d0, d1);
         }
-        // 128-byte swizzle: 16-byte unit u of row r sits at unit u ^ (r % 8)
-        uint8_t* chunk_row = ds_row + (cc / 2) * (kTileN * 128);
+        // 64 query columns = one 128-byte row of chunk h; 16-byte unit u of
+        // row r sits at unit u ^ (r % 8) (128-byte swizzle)
+        uint8_t* chunk_row = ds_row + h * (kTileN * 128);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int u = (cc % 2) * 4 + v;
+        for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(chunk_row + ((u ^ (r & 7)) << 4)) =
-              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-        }
+              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -422,35 +457,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // ===================== dQ: TMEM -> fp32 accumulator (one thread per query row) ====
+    // ===================== dQ: TMEM -> fp32 accumulator =====================
+    // d = 128: thread = head-dimension index, reading its dQ^T row (128 query
+    // columns); d = 64: thread = query row, reading its d values.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_dq = tmem + lane_off + 384;
+    constexpr int kCols = kDqT ? kTileM : D;
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
       if (!ok) break;
       tc_fence_after();
-      uint32_t acc[D];
+      uint32_t acc[kCols];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t raw[32];
-        tmem_ld32(t_dq + cc * 32, raw);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[cc * 32 + e] = raw[e];
-      }
+      for (int cc = 0; cc < kCols / 32; ++cc)
+        tmem_ld32(t_dq + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
       const int bh = bh_of(it), i = i_of(it);
-      float4* dst = reinterpret_cast<float4*>(
-          p.dq_acc + (static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM + r) * D);
+      float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM) * D;
+      if constexpr (kDqT) {
+        // warp-wide: 32 consecutive head-dimension entries of one query row
+        float* col = tile + r;
 #pragma unroll
-      for (int v = 0; v < D / 4; ++v)
-        atomicAdd(dst + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
-                                       __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
+        for (int q = 0; q < kTileM; ++q) atomicAdd(col + q * D, __uint_as_float(acc[q]));
+      } else {
+        float4* row = reinterpret_cast<float4*>(tile + static_cast<size_t>(r) * D);
+#pragma unroll
+        for (int v = 0; v < D / 4; ++v)
+          atomicAdd(row + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                         __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
+      }
     }
     // ---- epilogue: dV ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));

@@ -283,13 +283,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
+// Inverse of pack2 (exact): bf16 -> fp32 is a 16-bit shift; fp16 uses the
+// hardware conversion.
 template <bool kBf16>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
   if constexpr (kBf16) {
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
-    return __bfloat1622float2(h);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   } else {
-    __half2 h = *reinterpret_cast<__half2*>(&w);
+    __half2 h;
+    asm("mov.b32 %0, %1;" : "=r"(*reinterpret_cast<uint32_t*>(&h)) : "r"(w));
     return __half22float2(h);
   }
 }
