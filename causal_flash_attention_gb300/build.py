@@ -37,21 +37,29 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link libfa.so; returns its path. Raises on compiler errors."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False,
+          trace: bool = False) -> str:
+    """Compile and link libfa.so; returns its path. Raises on compiler errors.
+
+    trace=True builds libfa_trace.so instead: the same library compiled with
+    FA_TRACE, whose kernels record per-role timelines into a buffer set with
+    its extra export fa_trace_set(void*). The product library never has it.
+    """
+    bdir = BUILD + ("_trace" if trace else "")
+    lib = LIB.replace("libfa.so", "libfa_trace.so") if trace else LIB
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     headers = [os.path.join(CSRC, h) for h in HEADERS]
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         if force or _stale(o, [s] + headers):
-            cmd = [cc, *ARCH, *CFLAGS, "-c", s, "-o", o]
+            cmd = [cc, *ARCH, *CFLAGS, *(["-DFA_TRACE"] if trace else []), "-c", s, "-o", o]
             if ptxas_verbose:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -63,19 +71,19 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lrt",
                "-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if verbose or r.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         if r.returncode != 0:
-            raise RuntimeError("link of libfa.so failed")
-        os.replace(tmp, LIB)
-    return LIB
+            raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose=True, force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv)
-    print(LIB)
+    print(build(verbose=True, force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv,
+                trace="--trace" in sys.argv))

@@ -95,6 +95,16 @@ WsLayout ws_layout(int B, int Hq, int S, int d) {
 
 using namespace fa;
 
+#ifdef FA_TRACE
+// Trace builds only: the device buffer kernels record their timelines into
+// (kTraceCtas x kTraceRoles x kTraceSlots 64-bit entries), or null.
+static unsigned long long* g_trace_buf = nullptr;
+extern "C" void fa_trace_set(void* buf) { g_trace_buf = static_cast<unsigned long long*>(buf); }
+#define FA_TRACE_PTR g_trace_buf
+#else
+#define FA_TRACE_PTR nullptr
+#endif
+
 extern "C" {
 
 int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
@@ -150,6 +160,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
   p.causal = causal != 0;
   p.scale_log2 = scale * kLog2e;
   p.n_qpairs = (S + 2 * kTileM - 1) / (2 * kTileM);
+  p.trace = FA_TRACE_PTR;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   return launch_fwd_tc(p, d, bf16, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -222,6 +233,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out, const v
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.n_kv_tiles = (S + kTileN - 1) / kTileN;
+  p.trace = FA_TRACE_PTR;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   if (launch_bwd_tc(p, d, bf16, st) != cudaSuccess) return FA_ERR_CUDA;

@@ -229,11 +229,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sbase + Cfg::kOffV + c * (kTileN * 128), &p.tm_v, kv_full, c * kChunk,
                     j * kTileN, bkv);
       }
+      Tracer tr(p.trace, 0);
       int it = 0;
       for (; it < n_iter; ++it) {
         const int st = it % NS;
         const uint32_t use = static_cast<uint32_t>(it / NS);
         if (it >= NS && !mbar_wait(qdo_empty(st), (use - 1) & 1, abort_flag, p.status)) break;
+        tr(41);
         const int bh = bh_of(it), i = i_of(it);
         const uint32_t fb = qdo_full(st);
         mbar_arrive_expect_tx(fb, 2 * Cfg::kTileBytes + 1024);
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const size_t roff = static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM;
         bulk_load(sbase + Cfg::kOffRow + st * 1024, p.lse2 + roff, 512, fb);
         bulk_load(sbase + Cfg::kOffRow + st * 1024 + 512, p.delta + roff, 512, fb);
+        tr(40);
       }
       if (*abort_flag) {
         drain_wait(kv_full, 0, p.status);
@@ -289,8 +292,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_commit(dp_full);
       };
 
+      Tracer tr(p.trace, 1);
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.status) &&
                 mbar_wait(qdo_full(0), 0, abort_flag, p.status);
+      tr(9);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -302,6 +307,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool more = n + 1 < n_iter;
         // dV += P^T dO_i  (P^T from TMEM, 16-bit packed in S^T's first 64 columns)
         if (!(ok = mbar_wait(p_full, n & 1, abort_flag, p.status))) break;
+        tr(1);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTileM / 16; ++ks)
@@ -310,6 +316,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_commit(dv_done);
         // dK += dS^T Q_i
         if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, p.status))) break;
+        tr(3);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTileM / 16; ++ks)
@@ -322,6 +329,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                abort_flag, p.status)))
             break;
           if (!(ok = mbar_wait(dv_done, n & 1, abort_flag, p.status))) break;
+          tr(5);
           tc_fence_after();
           issue_s(st1);
         }
@@ -338,9 +346,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_commit(dq_full);
         tc_commit(ds_empty);
         tc_commit(qdo_empty(st));
+        tr(6);
         // dP^T for the next step, once dQ(n) has left TMEM
         if (more) {
           if (!(ok = mbar_wait(dq_empty, n & 1, abort_flag, p.status))) break;
+          tr(7);
           tc_fence_after();
           issue_dp(st1);
         }
@@ -358,6 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_dp = tmem + lane_off + 384;
     const float c = p.scale_log2;
     uint8_t* ds_row = smem + Cfg::kOffDS + r * 128;
+    Tracer tr((warp == 2 && lane == 0) ? p.trace : nullptr, 2);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int st = it % NS;
@@ -369,10 +380,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(qdo_full(st), par, abort_flag, p.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, p.status));
       if (!ok) break;
+      tr(20);
       tc_fence_after();
-      // masked: key past the end, or (causal) key after the query
-      const bool any_mask = (j * kTileN + kTileN > p.S) || (p.causal && i == j);
+      // Masked entries: key past the sequence end, or (causal) key after the
+      // query. Column qc of this row is masked iff qc < thr; thr <= 0 on every
+      // tile that is neither diagonal nor ragged, which skip the selects.
       const int q0 = i * kTileM;
+      const int thr = kv >= p.S ? kTileM : (p.causal ? min(kv - q0, kTileM) : 0);
+      const bool any_mask = __any_sync(0xffffffffu, thr > 0);
       uint32_t ppk[64];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -380,15 +395,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld32(t_s + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
         tmem_ld32(t_s + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
         tmem_wait_ld();
+        if (any_mask) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            raw[e] = (h * 64 + e < thr) ? __float_as_uint(-INFINITY) : raw[e];
+        }
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           const int qc = h * 64 + e;
-          float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[qc]));
-          float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[qc + 1]));
-          if (any_mask) {
-            if (kv >= p.S || (p.causal && kv > q0 + qc)) p0 = 0.f;
-            if (kv >= p.S || (p.causal && kv > q0 + qc + 1)) p1 = 0.f;
-          }
+          const float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[qc]));
+          const float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[qc + 1]));
           ppk[h * 32 + e / 2] = pack2<kBf16>(p0, p1);
         }
         tmem_st32(t_s + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(ppk + h * 32));
@@ -397,10 +413,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      tr(21);
 
       if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (it - 1) & 1, abort_flag, p.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag, p.status));
       if (!ok) break;
+      tr(22);
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -432,6 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(ds_full);
         mbar_arrive(qdo_empty(st));
       }
+      tr(23);
     }
     // ---- epilogue: dK = scale * accumulated dS^T Q ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
@@ -465,10 +484,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_dq = tmem + lane_off + 384;
     constexpr int kCols = kDqT ? kTileM : D;
+    Tracer tr((warp == 6 && lane == 0) ? p.trace : nullptr, 3);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
       if (!ok) break;
+      tr(30);
       tc_fence_after();
       uint32_t acc[kCols];
 #pragma unroll
@@ -478,6 +499,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
+      tr(31);
       const int bh = bh_of(it), i = i_of(it);
       float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM) * D;
       if constexpr (kDqT) {
@@ -492,6 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           atomicAdd(row + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
                                          __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
       }
+      tr(32);
     }
     // ---- epilogue: dV ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));

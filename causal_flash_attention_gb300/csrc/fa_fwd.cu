@@ -234,7 +234,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_commit(bars.pv(t));
       };
 
+      Tracer tr(p.trace, 1);
       if (ok) ok = mbar_wait(bars.kf(0), 0, abort_flag, p.status);
+      tr(9);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -248,6 +250,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= n_t[t]) continue;
           if (!(ok = mbar_wait(bars.pf(t), j & 1, abort_flag, p.status))) break;
+          tr(50 + t);
           tc_fence_after();
           issue_pv(t, st, j > 0);
           if (j + 1 < n_t[t]) {
@@ -256,6 +259,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!(ok = mbar_wait(bars.kf(st1), par1, abort_flag, p.status))) break;
             // P_t(j) lives in S_t's columns: wait until P_t(j) V_j has read it.
             if (!(ok = mbar_wait(bars.pv(t), j & 1, abort_flag, p.status))) break;
+            tr(54 + t);
             tc_fence_after();
             issue_qk(t, st1);
           }
@@ -283,12 +287,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t o_tmem = tmem + lane_off + 256 + t * 128;
     const float c = p.scale_log2;
 
+    Tracer tr(((warp == 2 || warp == 6) && lane == 0) ? p.trace : nullptr, 2 + t);
     float m_ref = -INFINITY;   // reference max, scaled log2 domain
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bars.sf(t), j & 1, abort_flag, p.status));
       if (!ok) break;
+      tr(60);
       tc_fence_after();
       float s[kTileN];
       {
@@ -362,6 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.pf(t));
+      tr(61);
     }
 
     if (ok && n > 0) {

@@ -26,6 +26,7 @@ struct FwdParams {
   float scale_log2;   // softmax scale * log2(e)
   int n_qpairs;       // ceil(S / 256): CTAs per (batch, query head)
   int* status;        // device status word (wait timeouts)
+  unsigned long long* trace;   // timeline buffer of trace builds (FA_TRACE); else null
 };
 
 struct BwdPreParams {
@@ -55,6 +56,7 @@ struct BwdParams {
   float scale_log2;   // softmax scale * log2(e)
   int n_kv_tiles;     // ceil(S / 128)
   int* status;
+  unsigned long long* trace;   // timeline buffer of trace builds (FA_TRACE); else null
 };
 
 struct DqConvertParams {

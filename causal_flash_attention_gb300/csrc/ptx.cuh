@@ -23,6 +23,33 @@ enum : int {
 // the GB300's SM clock) only ends a wait that would otherwise never finish.
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
+// ----------------------------------------------------------------- trace --
+// Timeline tracing, compiled in only when FA_TRACE is defined (a separate
+// trace build of the library). The first kTraceCtas CTAs of a launch record,
+// per role, up to kTraceSlots events as (clock64 << 8 | event id) into the
+// buffer passed in the kernel parameters. Without FA_TRACE the tracer is
+// empty and costs nothing.
+constexpr int kTraceCtas = 4, kTraceRoles = 4, kTraceSlots = 2048;
+#ifdef FA_TRACE
+struct Tracer {
+  unsigned long long* base = nullptr;
+  int n = 0;
+  __device__ Tracer(unsigned long long* buf, int role) {
+    if (buf && blockIdx.x < kTraceCtas)
+      base = buf + (static_cast<size_t>(blockIdx.x) * kTraceRoles + role) * kTraceSlots;
+  }
+  __device__ void operator()(int ev) {
+    if (base && n < kTraceSlots)
+      base[n++] = (static_cast<unsigned long long>(clock64()) << 8) | static_cast<unsigned>(ev);
+  }
+};
+#else
+struct Tracer {
+  __device__ Tracer(unsigned long long*, int) {}
+  __device__ void operator()(int) {}
+};
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -45,14 +72,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Test for completion of the phase with the given parity. A waiting thread is
+// suspended (issuing nothing) until the phase completes or about a
+// millisecond has passed, so waiting warps leave the issue slots to the
+// warps that compute.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
