@@ -81,10 +81,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {"fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"),
+                  "fa_bwd_kernel": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h")}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "causal_flash_attention_gb300", "csrc")
-    for name in ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -92,12 +96,13 @@ def kernel_source_hash():
 
 def recorded_traffic(kernel, workload):
     """DRAM bytes per launch recorded from an ncu capture in
-    profiles/dram_traffic.txt, valid only while the kernel sources hash the
-    same as when it was captured; else None."""
+    profiles/dram_traffic.txt (lines: kernel workload source-hash bytes ...),
+    valid only while the kernel's sources hash the same as when it was
+    captured; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and \
@@ -377,6 +382,8 @@ def main():
         else None
     peak = peaks["bf16_tflops"]
     traffic = recorded_traffic("fa_bwd_kernel", w.name)
+    if args.heads:
+        traffic = None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -399,6 +406,7 @@ def main():
         "roofline_fwd": {
             "kernel": "fa_fwd_kernel (one launch per fa_fwd call)", "bound": "tensor",
             "achieved": fwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
+            "traffic": None if args.heads else recorded_traffic("fa_fwd_kernel", w.name),
             "algorithmic_bytes": fwd_algorithmic_bytes(w),
         },
         "e2e": {"value": e2e_tf, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],

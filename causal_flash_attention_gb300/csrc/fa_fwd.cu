@@ -298,14 +298,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       float s[kTileN];
       {
-        uint32_t raw[32];
+        uint32_t raw[kTileN];
 #pragma unroll
-        for (int cc = 0; cc < kTileN / 32; ++cc) {
-          tmem_ld32(s_tmem + cc * 32, raw);
-          tmem_wait_ld();
+        for (int cc = 0; cc < kTileN / 32; ++cc)
+          tmem_ld32(s_tmem + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(raw + cc * 32));
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(raw[i]);
-        }
+        for (int i = 0; i < kTileN; ++i) s[i] = __uint_as_float(raw[i]);
       }
       const int kv0 = j * kTileN;
       // inline mask: causal (key > query) and keys past the sequence end
@@ -331,7 +330,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool moved = (m_new != m_ref);
       m_ref = m_new;
 
-      float sum0 = 0.f, sum1 = 0.f;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -339,13 +338,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int i = 0; i < 32; ++i) {
           const float p0 = ex2(fmaf(s[h * 64 + 2 * i], c, -m_use));
           const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], c, -m_use));
-          sum0 += p0;
-          sum1 += p1;
+          sum[(2 * i) & 3] += p0;
+          sum[(2 * i + 1) & 3] += p1;
           pk[i] = pack2<kBf16>(p0, p1);
         }
         tmem_st32(s_tmem + h * 32, pk);
       }
-      l = l * alpha + (sum0 + sum1);
+      l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
 
       // O <- alpha * O for rows whose reference max moved (not needed for the
       // first tile: its P V overwrites O)

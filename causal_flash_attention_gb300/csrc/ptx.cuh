@@ -72,18 +72,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Test for completion of the phase with the given parity. A waiting thread is
-// suspended (issuing nothing) until the phase completes or about a
-// millisecond has passed, so waiting warps leave the issue slots to the
-// warps that compute.
+// Test for completion of the phase with the given parity (the thread may be
+// held briefly inside the instruction). No suspend-time hint is passed: on the
+// critical paths here, a suspended waiter wakes later than a polling one.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
