@@ -32,6 +32,9 @@ import fa_inputs  # noqa: E402
 METRIC = "causal attention fwd/bwd TFLOP/s and % of GB300 dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+# ex2.approx.ftz.f32 results per clock per SM measured on the GB300 (one
+# 1024-thread block per SM, 16 independent chains per thread).
+EX2_PER_CLK_SM = 31.9
 
 
 # ------------------------------------------------------------ arithmetic --
@@ -202,9 +205,10 @@ def oracle_sample(w, head_inputs, rows):
     Q, K, V, DO = (x[:, :, :rows] for x in head_inputs)
     t0 = time.perf_counter()
     oracle.forward(Q, K, V, w.causal, w.scale)
-    oracle.backward(Q, K, V, DO, w.causal, w.scale)
+    if w.backward:
+        oracle.backward(Q, K, V, DO, w.causal, w.scale)
     dt = time.perf_counter() - t0
-    return dt, 7 * rows * rows * w.d
+    return dt, (7 if w.backward else 2) * rows * rows * w.d
 
 
 # ---------------------------------------------------------------- GPU arm --
@@ -230,7 +234,8 @@ def run_gpu(args, w, rank, world, local_rank):
 
     def step():
         fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale, stream)
-        fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
+        if w.backward:
+            fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
 
     def barrier():
         if dist is not None:
@@ -252,46 +257,84 @@ def run_gpu(args, w, rank, world, local_rank):
             ev[s][0].record(stream)
             fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale, stream)
             ev[s][1].record(stream)
-            fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
+            if w.backward:
+                fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
             ev[s][2].record(stream)
         barrier()
         total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
         fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
         bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
 
-        # end to end: pinned host inputs -> device, fwd + bwd, results -> pinned host
+        # End to end through the public API with host buffers: every step
+        # copies its inputs from pinned host memory, runs fa_fwd + fa_bwd and
+        # copies every result back to pinned host memory. Steps are pipelined
+        # over two device buffer sets: step k's host-to-device copies (one copy
+        # stream) and step k-1's device-to-host copies (another) overlap step
+        # k's kernels, as a caller streaming batches would run them.
         hq, hk, hv, hdo = (x.pin_memory() for x in (q, k, v, do))
         h_out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
         h_lse = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
         h_dq = torch.empty(q.shape, dtype=q.dtype).pin_memory()
         h_dk = torch.empty(k.shape, dtype=k.dtype).pin_memory()
         h_dv = torch.empty(v.shape, dtype=v.dtype).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
-        d2h = sum(x.numel() * x.element_size() for x in (h_out, h_lse, h_dq, h_dk, h_dv))
-
-        def e2e_step():
-            qd.copy_(hq, non_blocking=True)
-            kd.copy_(hk, non_blocking=True)
-            vd.copy_(hv, non_blocking=True)
-            dod.copy_(hdo, non_blocking=True)
-            step()
-            h_out.copy_(out, non_blocking=True)
-            h_lse.copy_(lse, non_blocking=True)
-            h_dq.copy_(dq, non_blocking=True)
-            h_dk.copy_(dk, non_blocking=True)
-            h_dv.copy_(dv, non_blocking=True)
-
+        ins_h = (hq, hk, hv, hdo) if w.backward else (hq, hk, hv)
+        outs_h = (h_out, h_lse, h_dq, h_dk, h_dv) if w.backward else (h_out, h_lse)
+        h2d = sum(x.numel() * x.element_size() for x in ins_h)
+        d2h = sum(x.numel() * x.element_size() for x in outs_h)
         K2 = 0 if args.no_e2e else max(3, K // 4)
-        for _ in range(2 if K2 else 0):
-            e2e_step()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K2):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        e2e_ms = e0.elapsed_time(e1) / K2 if K2 else float("nan")
+        if K2:
+            sets = []
+            for sidx in range(2):
+                if sidx == 0:
+                    ins_d = (qd, kd, vd, dod)
+                    outs_d = (out, lse, dq, dk, dv)
+                    ws_d = ws
+                else:
+                    ins_d = tuple(torch.empty_like(x) for x in (qd, kd, vd, dod))
+                    outs_d = tuple(torch.empty_like(x) for x in (out, lse, dq, dk, dv))
+                    ws_d = torch.empty_like(ws)
+                sets.append((ins_d, outs_d, ws_d))
+            s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+            ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set landed
+            ev_comp = [torch.cuda.Event() for _ in range(2)]   # kernels of set done
+            ev_out = [torch.cuda.Event() for _ in range(2)]    # results of set copied back
+            started = [False, False]
+
+            def e2e_step(kk):
+                sidx = kk % 2
+                (iq, ik, iv, ido), (oo, ol, oq, okk, ov), wsd = sets[sidx]
+                with torch.cuda.stream(s_h2d):
+                    if started[sidx]:
+                        s_h2d.wait_event(ev_comp[sidx])    # step k-2 has read this set
+                    for dst, src in zip((iq, ik, iv, ido), ins_h):
+                        dst.copy_(src, non_blocking=True)
+                    ev_in[sidx].record(s_h2d)
+                stream.wait_event(ev_in[sidx])
+                if started[sidx]:
+                    stream.wait_event(ev_out[sidx])        # step k-2's results copied out
+                fa.fa_fwd(iq, ik, iv, oo, ol, w.causal, w.scale, stream)
+                if w.backward:
+                    fa.fa_bwd(iq, ik, iv, oo, ido, ol, oq, okk, ov, wsd, w.causal, w.scale, stream)
+                ev_comp[sidx].record(stream)
+                with torch.cuda.stream(s_d2h):
+                    s_d2h.wait_event(ev_comp[sidx])
+                    for dst, src in zip(outs_h, (oo, ol, oq, okk, ov)):
+                        dst.copy_(src, non_blocking=True)
+                    ev_out[sidx].record(s_d2h)
+                started[sidx] = True
+
+            for kk in range(2):
+                e2e_step(kk)
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_h2d)
+            for kk in range(K2):
+                e2e_step(kk)
+            e1.record(s_d2h)
+            barrier()
+            e2e_ms = e0.elapsed_time(e1) / K2
+        else:
+            e2e_ms = float("nan")
     status = fa.fa_last_device_status(stream)
     if status:
         raise RuntimeError(f"device status {status} in the timed region")
@@ -409,24 +452,36 @@ def main():
             "traffic": None if args.heads else recorded_traffic("fa_fwd_kernel", w.name),
             "algorithmic_bytes": fwd_algorithmic_bytes(w),
         },
+        "exp_ceiling": {
+            "exps_per_step": w.B * w.Hq * w.S * (w.S + 1) // 2 if w.causal else w.B * w.Hq * w.S * w.S,
+            "ex2_per_clk_per_sm": EX2_PER_CLK_SM,
+            "fwd_floor_ms": (w.B * w.Hq * w.S * (w.S + 1) / 2) / (EX2_PER_CLK_SM * 152 * 2.07e9) * 1e3,
+            "note": "forward: one ex2 per visible score; floor at 152 SMs x 2.07 GHz",
+        },
         "e2e": {"value": e2e_tf, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
-        "gpu_launches": (1 + 3) * K,
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
+                "pipelining": "2 device buffer sets; H2D of step k and D2H of step k-1 on copy "
+                              "streams overlap step k's kernels"},
+        "gpu_launches": (4 if w.backward else 1) * K,
         "clocks": r["clocks"],
     }
+    if not w.backward:   # forward-only workload: the forward kernel is the whole step
+        line["roofline"] = dict(line["roofline_fwd"])
     if world == 1 and not args.no_cpu_baseline:
         cores, how = cpu_threads()
         total_t, total_f = 0.0, 0
+        rows = min(w.S, 8192)   # the dense oracle holds rows x rows float64 matrices
         for hin in oracle_inputs(w, 2):
-            dt, fl = oracle_sample(w, hin, w.S)
+            dt, fl = oracle_sample(w, hin, rows)
             total_t += dt
             total_f += fl
         line["cpu_baseline"] = {
             "value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores,
             "cores_source": how, "kind": "oracle",
-            "sample": f"fp64 dense forward + softmax-Jacobian backward of query heads 0 and 1 "
-                      f"(all {w.S} rows and keys) of {w.name}: {total_f / 1e9:.1f} GFLOP by "
-                      f"the causal convention in {total_t:.2f} s"}
+            "sample": f"fp64 dense forward{' + softmax-Jacobian backward' if w.backward else ''} "
+                      f"of the causal leading {rows}x{rows} block of query heads 0 and 1 of "
+                      f"{w.name} (all rows and keys when S = {rows}): "
+                      f"{total_f / 1e9:.1f} GFLOP by the causal convention in {total_t:.2f} s"}
     if r["dist"] is not None:
         r["dist"].destroy_process_group()
     print(json.dumps(line))

@@ -199,3 +199,50 @@ def test_repeat_calls_same_result(fa):
     assert np.array_equal(a["dk"], b["dk"]) and np.array_equal(a["dv"], b["dv"])
     # dQ is summed with atomics across key tiles: equal up to fp32 summation order
     assert np.abs(a["dq"] - b["dq"]).max() <= 1e-2 * np.abs(a["dq"]).max()
+
+
+# ------------------------------------------------------------ large sizes --
+def test_longest_sequence_sampled(fa):
+    """S = 65536 (twice the longest workload), one head, d = 64: forward and dQ
+    on sampled rows (dK/dV would need every row in the oracle)."""
+    B, H, S, d = 1, 1, 65536, 64
+    q, k, v, do = fa_inputs.make_custom(B, H, H, S, d, "bf16", seed=65)
+    scale = 1.0 / math.sqrt(d)
+    got = run_gpu(fa, q, k, v, do, True, scale)
+    Q, K, V, DO = map(f64, (q, k, v, do))
+    rows = fa_inputs.sample_rows(S, 48, seed=66)
+    o_r, l_r, dq_r = oracle.rows(Q, K, V, DO, 0, 0, rows, True, scale)
+    assert np.abs(got["out"][0, 0, rows] - o_r).max() <= OUT_TOL
+    assert np.abs(got["lse"][0, 0, rows] - l_r).max() <= LSE_TOL
+    check_grad("dq", got["dq"][0, 0, rows], dq_r)
+    assert np.isfinite(got["dk"]).all() and np.isfinite(got["dv"]).all()
+
+
+def test_many_heads_gqa(fa):
+    """1024 query heads in groups of 8 over 128 key/value heads."""
+    B, Hq, Hkv, S, d = 16, 64, 8, 256, 128
+    q, k, v, do = fa_inputs.make_custom(B, Hq, Hkv, S, d, "bf16", seed=1024)
+    scale = 1.0 / math.sqrt(d)
+    got = run_gpu(fa, q, k, v, do, True, scale)
+    Q, K, V, DO = map(f64, (q, k, v, do))
+    out_ref, lse_ref = oracle.forward(Q, K, V, True, scale)
+    check_fwd(got, out_ref, lse_ref)
+    dq, dk, dv = oracle.backward(Q, K, V, DO, True, scale)
+    check_grad("dq", got["dq"], dq)
+    check_grad("dk", got["dk"], dk)
+    check_grad("dv", got["dv"], dv)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+def test_non_causal_multi_tile(fa, dtype, d):
+    B, Hq, Hkv, S = 1, 4, 2, 1024
+    q, k, v, do = fa_inputs.make_custom(B, Hq, Hkv, S, d, dtype, seed=77 + d)
+    scale = 1.0 / math.sqrt(d)
+    got = run_gpu(fa, q, k, v, do, False, scale)
+    Q, K, V, DO = map(f64, (q, k, v, do))
+    out_ref, lse_ref = oracle.forward(Q, K, V, False, scale)
+    check_fwd(got, out_ref, lse_ref)
+    dq, dk, dv = oracle.backward(Q, K, V, DO, False, scale)
+    check_grad("dq", got["dq"], dq)
+    check_grad("dk", got["dk"], dk)
+    check_grad("dv", got["dv"], dv)
