@@ -211,26 +211,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc_pv = make_idesc(128, D, kBf16, false, true);
       bool ok = mbar_wait(bars.q_full, 0, abort_flag, p.status);
 
-      auto issue_qk = [&](int t, int st) {
-        const uint32_t qa = sbase + Cfg::kOffQ + t * Cfg::kTileBytes;
-        const uint32_t kb = sbase + Cfg::kOffK + st * Cfg::kTileBytes;
-        const uint32_t d_tmem = tmem + t * 128;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
-          mma_ss(d_tmem, make_sdesc(qa + off, 16, 1024), make_sdesc(kb + off, 16, 1024),
-                 idesc_qk, ks > 0);
-        }
+      auto issue_qk = [&](int t, int st) {   // S_t = Q_t K^T, both K-major
+        const uint64_t qa = make_sdesc(sbase + Cfg::kOffQ + t * Cfg::kTileBytes, 16, 1024);
+        const uint64_t kb = make_sdesc(sbase + Cfg::kOffK + st * Cfg::kTileBytes, 16, 1024);
+        mma_ss_product<D / 16, true, kTileM * 128, true, kTileN * 128>(tmem + t * 128, qa, kb,
+                                                                       idesc_qk, 0);
         tc_commit(bars.sf(t));
       };
-      auto issue_pv = [&](int t, int st, bool accumulate) {
-        const uint32_t vb = sbase + Cfg::kOffV + st * Cfg::kTileBytes;
-        const uint32_t p_tmem = tmem + t * 128;
-        const uint32_t o_tmem = tmem + 256 + t * 128;
-#pragma unroll
-        for (int ks = 0; ks < kTileN / 16; ++ks)
-          mma_ts(o_tmem, p_tmem + ks * 8, make_sdesc(vb + ks * 2048, kTileN * 128, 1024), idesc_pv,
-                 (accumulate || ks > 0) ? 1u : 0u);
+      auto issue_pv = [&](int t, int st, bool accumulate) {   // O_t (+)= P_t V
+        const uint64_t vb =
+            make_sdesc(sbase + Cfg::kOffV + st * Cfg::kTileBytes, kTileN * 128, 1024);
+        mma_ts_product8<false, 0>(tmem + 256 + t * 128, tmem + t * 128, vb, idesc_pv,
+                                  accumulate ? 1u : 0u);
         tc_commit(bars.pv(t));
       };
 

@@ -206,6 +206,105 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// ---- whole-product issue ---------------------------------------------------
+// One 128 x N x (16*STEPS) product as STEPS tcgen05.mma instructions in a
+// single asm block, with the per-step operand descriptors formed by adding
+// compile-time offsets to descriptors computed once. A single issuing thread
+// otherwise spends more time building descriptors than the tensor core spends
+// on an N = 128 step, and the tensor core sits idle in between.
+//
+// Offset of K-step ks in descriptor units (16 bytes), 128-byte swizzle:
+//   K-major:  32 bytes per step inside a 128-byte row, then the next
+//             64-element chunk (kChunkBytes further) every 4 steps;
+//   MN-major: 16 rows of 128 bytes (2048 bytes) per step.
+template <bool kKMajor, int kChunkBytes>
+__host__ __device__ constexpr int desc_step(int ks) {
+  return kKMajor ? ((ks % 4) * 2 + (ks / 4) * (kChunkBytes >> 4)) : ks * 128;
+}
+
+// D (+)= A B, both operands in shared memory. `accumulate` applies to the
+// first step; the remaining steps always accumulate.
+template <int STEPS, bool kAK, int kAC, bool kBK, int kBC>
+__device__ __forceinline__ void mma_ss_product(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                               uint32_t idesc, uint32_t accumulate) {
+  static_assert(STEPS == 4 || STEPS == 8, "4 or 8 K-steps");
+  if constexpr (STEPS == 4) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t}" ::"r"(d_tmem),
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate),
+        "n"(desc_step<kAK, kAC>(1)), "n"(desc_step<kBK, kBC>(1)),
+        "n"(desc_step<kAK, kAC>(2)), "n"(desc_step<kBK, kBC>(2)),
+        "n"(desc_step<kAK, kAC>(3)), "n"(desc_step<kBK, kBC>(3))
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %12;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %13;\n\tadd.s64 b, %2, %14;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %15;\n\tadd.s64 b, %2, %16;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+        "add.s64 a, %1, %17;\n\tadd.s64 b, %2, %18;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t}" ::"r"(d_tmem),
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate),
+        "n"(desc_step<kAK, kAC>(1)), "n"(desc_step<kBK, kBC>(1)),
+        "n"(desc_step<kAK, kAC>(2)), "n"(desc_step<kBK, kBC>(2)),
+        "n"(desc_step<kAK, kAC>(3)), "n"(desc_step<kBK, kBC>(3)),
+        "n"(desc_step<kAK, kAC>(4)), "n"(desc_step<kBK, kBC>(4)),
+        "n"(desc_step<kAK, kAC>(5)), "n"(desc_step<kBK, kBC>(5)),
+        "n"(desc_step<kAK, kAC>(6)), "n"(desc_step<kBK, kBC>(6)),
+        "n"(desc_step<kAK, kAC>(7)), "n"(desc_step<kBK, kBC>(7))
+        : "memory");
+  }
+}
+
+// D (+)= A B with A in tensor memory (16-bit, two per column: step ks reads
+// columns a_tmem + 8*ks) and B in shared memory; 8 K-steps.
+template <bool kBK, int kBC>
+__device__ __forceinline__ void mma_ts_product8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate),
+      "n"(desc_step<kBK, kBC>(1)), "n"(desc_step<kBK, kBC>(2)), "n"(desc_step<kBK, kBC>(3)),
+      "n"(desc_step<kBK, kBC>(4)), "n"(desc_step<kBK, kBC>(5)), "n"(desc_step<kBK, kBC>(6)),
+      "n"(desc_step<kBK, kBC>(7))
+      : "memory");
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
 //   1 = bf16), 15 A major, 16 B major (0 = K-major, 1 = MN-major),
