@@ -14,8 +14,14 @@ Workloads (shapes in [B, H, S, d] order, Q/dO with Hq heads, K/V with Hkv):
   long_8k      bf16,  B=1 Hq=Hkv=32 S=8192  d=128, 0.5*N(0,1) with every
                512th key (positions 0, 512, 1024, ...) scaled by 8, seed 3
   fp16_32k     fp16,  B=1 Hq=Hkv=8  S=32768 d=64,  N(0,1), seed 4, forward only
+  gqa_qwen3_nc gqa_qwen3 without the causal mask (same draws)
+  long_8k_nc   long_8k without the causal mask (same draws)
+  prefill_8k   bf16,  B=1 Hq=32 Hkv=8 Sq=2048 Skv=8192 d=128, N(0,1), seed 5:
+               a 2048-query chunk at the end of an 8192-position context
+               (causal mask aligned to the last key, kv_offset = Skv - Sq)
 
-All use causal masking and scale = 1/sqrt(d).
+All use scale = 1/sqrt(d); all but the *_nc workloads use causal masking.
+S is the query length; K and V have `kv_len` rows (S unless Skv is given).
 """
 from __future__ import annotations
 
@@ -42,6 +48,11 @@ class Workload:
     value_scale: float = 1.0      # multiplies every N(0,1) draw
     spike_every: int = 0          # if > 0: K rows at positions % spike_every == 0 ...
     spike_scale: float = 1.0      # ... are multiplied by this before rounding
+    Skv: int = 0                  # key/value length; 0 means the same as S
+
+    @property
+    def kv_len(self) -> int:
+        return self.Skv or self.S
 
     @property
     def scale(self) -> float:
@@ -52,8 +63,9 @@ class Workload:
         return DTYPES[self.dtype]
 
     def describe(self) -> str:
+        lens = f"S={self.S}" if self.kv_len == self.S else f"Sq={self.S} Skv={self.kv_len}"
         s = (f"{self.name}: {self.dtype} B={self.B} Hq={self.Hq} Hkv={self.Hkv} "
-             f"S={self.S} d={self.d} causal={int(self.causal)} seed={self.seed}")
+             f"{lens} d={self.d} causal={int(self.causal)} seed={self.seed}")
         if self.value_scale != 1.0:
             s += f" values={self.value_scale}*N(0,1)"
         if self.spike_every:
@@ -70,6 +82,10 @@ WORKLOADS = {
         Workload("long_8k", "bf16", 1, 32, 32, 8192, 128, seed=3,
                  value_scale=0.5, spike_every=512, spike_scale=8.0),
         Workload("fp16_32k", "fp16", 1, 8, 8, 32768, 64, seed=4, backward=False),
+        Workload("gqa_qwen3_nc", "bf16", 4, 32, 8, 2048, 128, seed=2, causal=False),
+        Workload("long_8k_nc", "bf16", 1, 32, 32, 8192, 128, seed=3, causal=False,
+                 value_scale=0.5, spike_every=512, spike_scale=8.0),
+        Workload("prefill_8k", "bf16", 1, 32, 8, 2048, 128, seed=5, Skv=8192),
     ]
 }
 
@@ -84,7 +100,7 @@ def make_inputs(w: Workload, with_dout: bool = True):
     """
     g = torch.Generator().manual_seed(w.seed)
     qshape = (w.B, w.Hq, w.S, w.d)
-    kshape = (w.B, w.Hkv, w.S, w.d)
+    kshape = (w.B, w.Hkv, w.kv_len, w.d)
 
     def draw(shape):
         t = torch.randn(shape, generator=g, dtype=torch.float32)
@@ -104,10 +120,11 @@ def make_inputs(w: Workload, with_dout: bool = True):
 
 
 def make_custom(B, Hq, Hkv, S, d, dtype="bf16", seed=0, value_scale=1.0,
-                with_dout=True):
-    """Same recipe as `make_inputs` for an ad-hoc shape (edge-case tests)."""
+                with_dout=True, Skv=0):
+    """Same recipe as `make_inputs` for an ad-hoc shape (edge-case tests);
+    S is the query length, Skv the key/value length (0: same as S)."""
     w = Workload("custom", dtype, B, Hq, Hkv, S, d, seed=seed,
-                 value_scale=value_scale)
+                 value_scale=value_scale, Skv=Skv)
     return make_inputs(w, with_dout=with_dout)
 
 

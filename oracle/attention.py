@@ -8,8 +8,10 @@ and the CUDA path never calls it.
 Inputs are numpy float64 arrays holding the values the GPU sees (bf16 / fp16 /
 fp32 tensors widened exactly to double):
 
-    q, dout : [B, Hq,  S, d]
-    k, v    : [B, Hkv, S, d]        Hq % Hkv == 0, G = Hq // Hkv
+    q, dout : [B, Hq,  Sq,  d]
+    k, v    : [B, Hkv, Skv, d]      Hq % Hkv == 0, G = Hq // Hkv
+
+Sq and Skv are the query and key/value lengths (equal in self-attention).
 
 Query head h reads key/value head h // G (grouped-query attention, as in
 "Phase 14: Flash Attention 2 for SM120", section "GQA 支持"). dK and dV of a
@@ -21,7 +23,13 @@ What is computed (the plain definition, no tiling):
     key position j > query position i ("Phase T14: 融合 Flash-Attention
     Kernel", section "什么是 flash-attention": standard attention
     O = softmax(causal(Q K^T / sqrt(d))) V, masked columns j > i; "FlashAttention
-    与 SDPA Backend", section "先从 reference 语义出发").
+    与 SDPA Backend", section "先从 reference 语义出发"). When the key/value
+    sequence is longer than the query sequence, query row i sits at position
+    i + kv_offset with kv_offset = Skv - Sq, so the mask is j > i + kv_offset
+    ("Phase 14: Flash Attention 2 for SM120", section "Causal Mask": the offset
+    is kv_len - q_len, for a KV cache longer than Q). Causal masking needs
+    Skv >= Sq: with fewer keys than queries the first rows would see no key at
+    all and their softmax would be undefined.
   * P = row softmax of s, O = P V, and the natural-log logsumexp
     LSE_i = log sum_j exp(s_ij), the per-row statistic the forward keeps for
     the backward ("Phase T14", section "Key Design Decisions" item 2, L = m + log l).
@@ -45,18 +53,22 @@ from __future__ import annotations
 import numpy as np
 
 
-def _check(q, k, v):
+def _check(q, k, v, causal=False):
+    """Returns (B, Hq, Hkv, Sq, Skv, d)."""
     if q.ndim != 4 or k.shape != v.shape or q.shape[0] != k.shape[0] or \
-            q.shape[2:] != k.shape[2:] or q.shape[1] % k.shape[1] != 0:
+            q.shape[3] != k.shape[3] or q.shape[1] % k.shape[1] != 0:
         raise ValueError(f"bad shapes q{q.shape} k{k.shape} v{v.shape}")
-    return q.shape[0], q.shape[1], k.shape[1], q.shape[2], q.shape[3]
+    if causal and k.shape[2] < q.shape[2]:
+        raise ValueError("causal masking needs at least as many keys as queries")
+    return q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3]
 
 
-def _causal_mask(n_rows, n_cols, row0=0):
-    """True where key position j > query position i (masked)."""
+def _causal_mask(n_rows, n_cols, row0=0, offset=0):
+    """True where key position j > query position i + offset (masked); the
+    rows are query rows row0 .. row0 + n_rows - 1."""
     rows = np.arange(row0, row0 + n_rows)[:, None]
     cols = np.arange(n_cols)[None, :]
-    return cols > rows
+    return cols > rows + offset
 
 
 def _softmax_rows(s):
@@ -69,21 +81,21 @@ def _softmax_rows(s):
 
 
 def head_probs(qh, kh, causal, scale):
-    """Probabilities P [S, S] and LSE [S] of one (batch, query head)."""
+    """Probabilities P [Sq, Skv] and LSE [Sq] of one (batch, query head)."""
     s = scale * (qh @ kh.T)
     if causal:
-        s[_causal_mask(*s.shape)] = -np.inf
+        s[_causal_mask(*s.shape, offset=kh.shape[0] - qh.shape[0])] = -np.inf
     p, m, l = _softmax_rows(s)
     return p, m + np.log(l)
 
 
 def forward(q, k, v, causal=True, scale=None):
-    """Dense forward: returns (out [B,Hq,S,d], lse [B,Hq,S]) in float64."""
-    B, Hq, Hkv, S, d = _check(q, k, v)
+    """Dense forward: returns (out [B,Hq,Sq,d], lse [B,Hq,Sq]) in float64."""
+    B, Hq, Hkv, Sq, _, d = _check(q, k, v, causal)
     G = Hq // Hkv
     scale = 1.0 / np.sqrt(d) if scale is None else scale
-    out = np.empty((B, Hq, S, d))
-    lse = np.empty((B, Hq, S))
+    out = np.empty((B, Hq, Sq, d))
+    lse = np.empty((B, Hq, Sq))
     for b in range(B):
         for h in range(Hq):
             p, lse[b, h] = head_probs(q[b, h], k[b, h // G], causal, scale)
@@ -105,12 +117,12 @@ def _jacobian_vjp(p, dp):
 def backward(q, k, v, dout, causal=True, scale=None):
     """Dense backward: returns (dq, dk, dv) in float64 (dk/dv summed over each
     key/value head's query-head group)."""
-    B, Hq, Hkv, S, d = _check(q, k, v)
+    B, Hq, Hkv, Sq, Skv, d = _check(q, k, v, causal)
     G = Hq // Hkv
     scale = 1.0 / np.sqrt(d) if scale is None else scale
-    dq = np.zeros((B, Hq, S, d))
-    dk = np.zeros((B, Hkv, S, d))
-    dv = np.zeros((B, Hkv, S, d))
+    dq = np.zeros((B, Hq, Sq, d))
+    dk = np.zeros((B, Hkv, Skv, d))
+    dv = np.zeros((B, Hkv, Skv, d))
     for b in range(B):
         for h in range(Hq):
             kvh = h // G
@@ -135,24 +147,27 @@ def forward_tiled(q, k, v, causal=True, scale=None, block_n=64):
     acc = acc*exp(m - m_new) + p V_tile; finally out = acc / l and
     LSE = m + log l. Masked entries contribute p = 0.
 
+    Query row i stands at position i + kv_offset, kv_offset = Skv - Sq
+    ("Phase 14", section "Causal Mask").
+
     Returns (out, lse, m, l), all float64.
     """
-    B, Hq, Hkv, S, d = _check(q, k, v)
+    B, Hq, Hkv, Sq, Skv, d = _check(q, k, v, causal)
     G = Hq // Hkv
     scale = 1.0 / np.sqrt(d) if scale is None else scale
-    out = np.empty((B, Hq, S, d))
-    lse = np.empty((B, Hq, S))
-    m_all = np.empty((B, Hq, S))
-    l_all = np.empty((B, Hq, S))
-    query_pos = np.arange(S)[:, None]
+    out = np.empty((B, Hq, Sq, d))
+    lse = np.empty((B, Hq, Sq))
+    m_all = np.empty((B, Hq, Sq))
+    l_all = np.empty((B, Hq, Sq))
+    query_pos = np.arange(Sq)[:, None] + (Skv - Sq)
     for b in range(B):
         for h in range(Hq):
             qh, kh, vh = q[b, h], k[b, h // G], v[b, h // G]
-            m = np.full(S, -np.inf)
-            l = np.zeros(S)
-            acc = np.zeros((S, d))
-            for start in range(0, S, block_n):
-                end = min(start + block_n, S)
+            m = np.full(Sq, -np.inf)
+            l = np.zeros(Sq)
+            acc = np.zeros((Sq, d))
+            for start in range(0, Skv, block_n):
+                end = min(start + block_n, Skv)
                 s = scale * (qh @ kh[start:end].T)
                 if causal:
                     key_pos = np.arange(start, end)[None, :]
@@ -176,10 +191,11 @@ def forward_tiled(q, k, v, causal=True, scale=None, block_n=64):
 def rows(q, k, v, dout, b, h, idx, causal=True, scale=None):
     """Forward and dQ of selected query rows of one (batch, query head).
 
-    Row i needs only keys 0..i under causal masking (all keys otherwise), so
-    this is O(S d) per row. Returns (out [n,d], lse [n], dq [n,d]).
+    Row i needs only keys 0..i + kv_offset under causal masking (all keys
+    otherwise), so this is O(Skv d) per row. Returns (out [n,d], lse [n],
+    dq [n,d]).
     """
-    _, Hq, Hkv, S, d = _check(q, k, v)
+    _, Hq, Hkv, Sq, Skv, d = _check(q, k, v, causal)
     G = Hq // Hkv
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     kh, vh = k[b, h // G], v[b, h // G]
@@ -187,7 +203,7 @@ def rows(q, k, v, dout, b, h, idx, causal=True, scale=None):
     lse = np.empty(len(idx))
     dq = np.empty((len(idx), d))
     for n, i in enumerate(idx):
-        visible = i + 1 if causal else S
+        visible = i + 1 + (Skv - Sq) if causal else Skv
         s = scale * (kh[:visible] @ q[b, h, i])
         p, m, l = _softmax_rows(s[None, :])
         out[n] = p[0] @ vh[:visible]
@@ -208,23 +224,25 @@ def key_columns(q, k, v, dout, b, kvh, idx, causal=True, scale=None,
     is evaluated; rows are taken `row_block` at a time to bound memory.
     Returns (dk [n,d], dv [n,d]).
     """
-    _, Hq, Hkv, S, d = _check(q, k, v)
+    _, Hq, Hkv, Sq, Skv, d = _check(q, k, v, causal)
     G = Hq // Hkv
     scale = 1.0 / np.sqrt(d) if scale is None else scale
+    off = Skv - Sq
     idx = np.asarray(idx)
     kh, vh = k[b, kvh], v[b, kvh]
     dk = np.zeros((len(idx), d))
     dv = np.zeros((len(idx), d))
     for h in range(kvh * G, (kvh + 1) * G):
-        for r0 in range(0, S, row_block):
-            r1 = min(r0 + row_block, S)
-            ncol = r1 if causal else S          # keys beyond r1-1 are masked
+        for r0 in range(0, Sq, row_block):
+            r1 = min(r0 + row_block, Sq)
+            # keys beyond position r1 - 1 + kv_offset are masked for these rows
+            ncol = r1 + off if causal else Skv
             sel = idx < ncol
             if not sel.any():
                 continue
             s = scale * (q[b, h, r0:r1] @ kh[:ncol].T)
             if causal:
-                s[_causal_mask(r1 - r0, ncol, r0)] = -np.inf
+                s[_causal_mask(r1 - r0, ncol, r0, off)] = -np.inf
             p, _, _ = _softmax_rows(s)
             dp = dout[b, h, r0:r1] @ vh[:ncol].T
             ds = _jacobian_vjp(p, dp)

@@ -7,6 +7,7 @@ own CPU attention in float64), central finite differences, and brute force on
 tiny inputs. `test_planted_mistakes_are_caught` plants plausible mistakes in
 the oracle and checks that these pins catch them.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -270,6 +271,7 @@ def _pins_pass():
         for causal in (True, False):
             test_matches_torch_sdpa_float64((1, 2, 2, 40, 8), causal)
         test_finite_differences(1, 2, 1, 5, 4, True)
+        test_kv_offset_matches_torch_lower_right_bias((1, 2, 1, 5, 12, 4), True)
     except Exception:   # a failed assertion, or NaNs tripping a comparison
         return False
     return True
@@ -285,9 +287,13 @@ def test_planted_mistakes_are_caught(monkeypatch):
     assert _pins_pass()
     mutants = {
         "mask includes the diagonal": ("_causal_mask",
-            lambda n, c, r0=0: np.arange(c)[None, :] >= np.arange(r0, r0 + n)[:, None]),
+            lambda n, c, r0=0, offset=0: np.arange(c)[None, :] >= np.arange(r0, r0 + n)[:, None] + offset),
         "mask off by one the other way": ("_causal_mask",
-            lambda n, c, r0=0: np.arange(c)[None, :] > np.arange(r0, r0 + n)[:, None] + 1),
+            lambda n, c, r0=0, offset=0: np.arange(c)[None, :] > np.arange(r0, r0 + n)[:, None] + offset + 1),
+        "kv_offset ignored (top-left alignment)": ("_causal_mask",
+            lambda n, c, r0=0, offset=0: np.arange(c)[None, :] > np.arange(r0, r0 + n)[:, None]),
+        "kv_offset with the wrong sign": ("_causal_mask",
+            lambda n, c, r0=0, offset=0: np.arange(c)[None, :] > np.arange(r0, r0 + n)[:, None] - offset),
         "Jacobian term dropped": ("_jacobian_vjp", lambda p, dp: p * dp),
         "Jacobian sign flipped": ("_jacobian_vjp",
             lambda p, dp: p * dp + p * (p * dp).sum(axis=1, keepdims=True)),
@@ -311,3 +317,155 @@ def test_workload_recipes():
     assert w.S == 8192 and w.d == 128 and w.Hq == w.Hkv == 32
     rows = fa_inputs.sample_rows(8192, 256, seed=0)
     assert len(rows) == 256 and {0, 127, 128, 511, 512, 8191} <= set(rows)
+
+
+# 10. separate query and key/value lengths. Query row i stands at position
+#     i + kv_offset, kv_offset = Skv - Sq ("Phase 14: Flash Attention 2 for
+#     SM120", section "Causal Mask"), i.e. the causal mask is aligned to the
+#     last key. PyTorch's `causal_lower_right` attention bias is an independent
+#     definition of exactly that alignment.
+def rand_qkv_kv(B, Hq, Hkv, Sq, Skv, d):
+    rng = np.random.default_rng(B * 7919 + Hq * 131 + Sq * 17 + Skv * 3 + d)
+    return (rand(B, Hq, Sq, d, rng=rng), rand(B, Hkv, Skv, d, rng=rng),
+            rand(B, Hkv, Skv, d, rng=rng), rand(B, Hq, Sq, d, rng=rng))
+
+
+KV_SHAPES = [(1, 2, 2, 1, 9, 8), (1, 2, 1, 5, 12, 4), (2, 4, 2, 17, 40, 8),
+             (1, 2, 2, 33, 33, 8), (1, 1, 1, 3, 130, 4)]
+
+
+@pytest.mark.parametrize("shape", KV_SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_kv_offset_matches_torch_lower_right_bias(shape, causal):
+    from torch.nn.attention.bias import causal_lower_right
+    B, Hq, Hkv, Sq, Skv, d = shape
+    q, k, v, do = rand_qkv_kv(*shape)
+    scale = 0.7
+    out, lse = oracle.forward(q, k, v, causal, scale)
+    dq, dk, dv = oracle.backward(q, k, v, do, causal, scale)
+
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    G = Hq // Hkv
+    tk_rep = tk.repeat_interleave(G, dim=1)
+    tv_rep = tv.repeat_interleave(G, dim=1)
+    bias = causal_lower_right(Sq, Skv) if causal else None
+    tout = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk_rep, tv_rep, attn_mask=bias, scale=scale)
+    tout.backward(torch.tensor(do))
+    sc = (tq @ tk_rep.transpose(-1, -2)) * scale
+    if causal:
+        sc = sc.masked_fill(~bias._materialize(), -math.inf)
+    tlse = torch.logsumexp(sc, dim=-1)
+
+    assert np.abs(out - tout.detach().numpy()).max() <= 1e-12
+    assert np.abs(lse - tlse.detach().numpy()).max() <= 1e-12
+    assert np.abs(dq - tq.grad.numpy()).max() <= 1e-12
+    assert np.abs(dk - tk.grad.numpy()).max() <= 1e-12
+    assert np.abs(dv - tv.grad.numpy()).max() <= 1e-12
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 1, 5, 12, 4), (2, 4, 2, 17, 40, 8)])
+def test_query_chunk_is_the_tail_of_self_attention(shape):
+    """A chunk of the last Sq queries against all Skv keys gives the last Sq
+    rows of self-attention over Skv positions, forward and backward (with dO
+    zero on the rows outside the chunk)."""
+    B, Hq, Hkv, Sq, Skv, d = shape
+    rng = np.random.default_rng(99)
+    q_full = rand(B, Hq, Skv, d, rng=rng)
+    k, v = rand(B, Hkv, Skv, d, rng=rng), rand(B, Hkv, Skv, d, rng=rng)
+    do = rand(B, Hq, Sq, d, rng=rng)
+    tail = slice(Skv - Sq, Skv)
+    out_c, lse_c = oracle.forward(q_full[:, :, tail], k, v, True)
+    out_f, lse_f = oracle.forward(q_full, k, v, True)
+    assert np.abs(out_c - out_f[:, :, tail]).max() <= 1e-13
+    assert np.abs(lse_c - lse_f[:, :, tail]).max() <= 1e-13
+    do_full = np.zeros_like(q_full)
+    do_full[:, :, tail] = do
+    dq_c, dk_c, dv_c = oracle.backward(q_full[:, :, tail], k, v, do, True)
+    dq_f, dk_f, dv_f = oracle.backward(q_full, k, v, do_full, True)
+    assert np.abs(dq_c - dq_f[:, :, tail]).max() <= 1e-13
+    assert np.abs(dk_c - dk_f).max() <= 1e-13
+    assert np.abs(dv_c - dv_f).max() <= 1e-13
+
+
+def test_single_query_sees_every_key():
+    """Sq = 1 (one new token against a longer key/value sequence): the causal
+    mask hides nothing, so the result is the unmasked one."""
+    q, k, v, do = rand_qkv_kv(1, 2, 1, 1, 37, 8)
+    for a, b in zip(oracle.forward(q, k, v, True), oracle.forward(q, k, v, False)):
+        assert np.array_equal(a, b)
+    for a, b in zip(oracle.backward(q, k, v, do, True), oracle.backward(q, k, v, do, False)):
+        assert np.array_equal(a, b)
+
+
+def test_causal_needs_keys_for_every_query():
+    q, k, v, do = rand_qkv_kv(1, 1, 1, 9, 4, 4)
+    with pytest.raises(ValueError):
+        oracle.forward(q, k, v, True)
+    out, lse = oracle.forward(q, k, v, False)      # unmasked: any lengths
+    assert out.shape == (1, 1, 9, 4) and np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("shape", KV_SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("block_n", [1, 3, 64])
+def test_tiled_matches_dense_kv_lengths(shape, causal, block_n):
+    q, k, v, _ = rand_qkv_kv(*shape)
+    out, lse = oracle.forward(q, k, v, causal)
+    out_t, lse_t, _, _ = oracle.forward_tiled(q, k, v, causal, block_n=block_n)
+    assert np.abs(out - out_t).max() <= 1e-12
+    assert np.abs(lse - lse_t).max() <= 1e-12
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_finite_differences_kv_lengths(causal):
+    q, k, v, w = rand_qkv_kv(1, 2, 1, 3, 7, 4)
+    scale = 0.8
+
+    def F(q_, k_, v_):
+        return float((w * oracle.forward(q_, k_, v_, causal, scale)[0]).sum())
+
+    dq, dk, dv = oracle.backward(q, k, v, w, causal, scale)
+    eps = 1e-6
+    for x, g, pos in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args = [q, k, v]
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args[pos] = xp
+            fp = F(*args)
+            args[pos] = xm
+            fm = F(*args)
+            num[idx] = (fp - fm) / (2 * eps)
+        assert np.abs(num - g).max() <= 1e-7 * max(1.0, np.abs(g).max())
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_sampled_evaluators_kv_lengths(causal):
+    q, k, v, do = rand_qkv_kv(1, 4, 2, 150, 420, 8)
+    out, lse = oracle.forward(q, k, v, causal)
+    dq, dk, dv = oracle.backward(q, k, v, do, causal)
+    qidx = fa_inputs.sample_rows(150, 20, seed=6)
+    kidx = fa_inputs.sample_rows(420, 30, seed=7)
+    for h in (0, 3):
+        o_r, l_r, dq_r = oracle.rows(q, k, v, do, 0, h, qidx, causal)
+        assert np.abs(o_r - out[0, h, qidx]).max() <= 1e-13
+        assert np.abs(l_r - lse[0, h, qidx]).max() <= 1e-13
+        assert np.abs(dq_r - dq[0, h, qidx]).max() <= 1e-12
+    for kvh in (0, 1):
+        dk_c, dv_c = oracle.key_columns(q, k, v, do, 0, kvh, kidx, causal, row_block=64)
+        assert np.abs(dk_c - dk[0, kvh, kidx]).max() <= 1e-12
+        assert np.abs(dv_c - dv[0, kvh, kidx]).max() <= 1e-12
+
+
+def test_kv_length_workload_recipes():
+    w = fa_inputs.WORKLOADS["prefill_8k"]
+    assert (w.S, w.kv_len, w.Hq, w.Hkv, w.d, w.causal) == (2048, 8192, 32, 8, 128, True)
+    small = fa_inputs.Workload("t", "bf16", 1, 4, 2, 10, 8, seed=5, Skv=30)
+    q, k, v, do = fa_inputs.make_inputs(small)
+    assert q.shape == do.shape == (1, 4, 10, 8) and k.shape == v.shape == (1, 2, 30, 8)
+    for name in ("long_8k_nc", "gqa_qwen3_nc"):
+        nc, c = fa_inputs.WORKLOADS[name], fa_inputs.WORKLOADS[name[:-3]]
+        assert not nc.causal and dataclasses.replace(nc, name=c.name, causal=True) == c
