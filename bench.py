@@ -6,7 +6,11 @@ A step is one pass of the whole path over one batch: fa_fwd (out, lse) then
 fa_bwd (dq, dk, dv) through the C ABI on the long_8k workload (bf16, B=1,
 Hq=Hkv=32, S=8192, d=128, causal, synthetic seeded inputs with spike keys).
 FLOPs follow the causal convention 2*B*Hq*S^2*d (forward) + 5*B*Hq*S^2*d
-(backward). Each rank runs its own replica (no collective on the data path);
+(backward), i.e. 4*d (forward) and 10*d (backward) per visible query-key pair
+with S^2/2 visible pairs per head; unmasked workloads count Sq*Skv pairs and
+a causal query chunk (Sq < Skv, mask aligned to the last key) Sq*Skv - Sq^2/2.
+Other workloads (--workload) are timed the same way. Each rank runs its own
+replica (no collective on the data path);
 `value` is the FLOPs of all ranks divided by the slowest rank's time.
 
 Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle
@@ -38,10 +42,17 @@ EX2_PER_CLK_SM = 31.9
 
 
 # ------------------------------------------------------------ arithmetic --
+def visible_pairs(Sq, Skv, causal):
+    """Query-key pairs per head that the mask leaves visible, by the FLOP
+    convention (S^2/2 for causal self-attention)."""
+    return Sq * Skv - Sq * Sq / 2 if causal else Sq * Skv
+
+
 def flops(w, fwd=True, bwd=True):
-    """Causal FLOP convention: forward 2*B*Hq*S^2*d, backward 5*B*Hq*S^2*d."""
-    base = w.B * w.Hq * w.S * w.S * w.d
-    return (2 * base if fwd else 0) + (5 * base if bwd else 0)
+    """FLOP convention: 4*d per visible pair forward (two GEMMs), 10*d backward
+    (five GEMMs); causal self-attention gives 2*B*Hq*S^2*d and 5*B*Hq*S^2*d."""
+    base = w.B * w.Hq * visible_pairs(w.S, w.kv_len, w.causal) * w.d
+    return (4 * base if fwd else 0) + (10 * base if bwd else 0)
 
 
 def elem_bytes(w):
@@ -61,7 +72,7 @@ def score_matrix_bytes(B, H, S, esize):
 def fwd_algorithmic_bytes(w):
     """Compulsory HBM traffic of one forward: read Q, K, V, write O and LSE."""
     e = elem_bytes(w)
-    return (2 * tensor_bytes(w.B, w.Hq, w.S, w.d, e) + 2 * tensor_bytes(w.B, w.Hkv, w.S, w.d, e)
+    return (2 * tensor_bytes(w.B, w.Hq, w.S, w.d, e) + 2 * tensor_bytes(w.B, w.Hkv, w.kv_len, w.d, e)
             + w.B * w.Hq * w.S * 4)
 
 
@@ -70,7 +81,7 @@ def bwd_algorithmic_bytes(w):
     dQ, dK, dV."""
     e = elem_bytes(w)
     q = tensor_bytes(w.B, w.Hq, w.S, w.d, e)
-    kv = tensor_bytes(w.B, w.Hkv, w.S, w.d, e)
+    kv = tensor_bytes(w.B, w.Hkv, w.kv_len, w.d, e)
     return 4 * q + 4 * kv + w.B * w.Hq * w.S * 4
 
 
@@ -196,19 +207,29 @@ def oracle_inputs(w, heads):
              f64(do[:1, h:h + 1])) for h in range(heads)]
 
 
-def oracle_sample(w, head_inputs, rows):
-    """Time the fp64 oracle's dense forward + backward on the causal leading
-    block (query rows and keys 0..rows-1) of one head of workload `w`. Under the
-    causal mask those rows see only those keys, so this is an exact piece of the
-    full problem. Returns (seconds, causal-convention flops 7*rows^2*d)."""
+def oracle_block(w, max_rows):
+    """The leading block the oracle samples: query rows 0..r-1 and the keys
+    they see (causal: keys up to row position r-1 + kv_offset; unmasked: all
+    keys). Under the causal mask this is an exact piece of the full problem."""
+    r = min(w.S, max_rows)
+    kv = min(w.kv_len, r + w.kv_len - w.S) if w.causal else w.kv_len
+    return r, kv
+
+
+def oracle_sample(w, head_inputs, block):
+    """Time the fp64 oracle's dense forward + backward on `block` (rows, keys)
+    of one head of workload `w`. Returns (seconds, flops of that block by the
+    same convention)."""
     import oracle
-    Q, K, V, DO = (x[:, :, :rows] for x in head_inputs)
+    r, kv = block
+    Q, DO = (x[:, :, :r] for x in (head_inputs[0], head_inputs[3]))
+    K, V = (x[:, :, :kv] for x in (head_inputs[1], head_inputs[2]))
     t0 = time.perf_counter()
     oracle.forward(Q, K, V, w.causal, w.scale)
     if w.backward:
         oracle.backward(Q, K, V, DO, w.causal, w.scale)
     dt = time.perf_counter() - t0
-    return dt, (7 if w.backward else 2) * rows * rows * w.d
+    return dt, (14 if w.backward else 4) * visible_pairs(r, kv, w.causal) * w.d
 
 
 # ---------------------------------------------------------------- GPU arm --
@@ -231,11 +252,14 @@ def run_gpu(args, w, rank, world, local_rank):
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     ws = fa.workspace_for(qd, kd)
     stream = torch.cuda.current_stream(dev)
+    # self-attention through fa_fwd / fa_bwd; separate lengths through the *_kv calls
+    fwd_call = fa.fa_fwd if w.S == w.kv_len else fa.fa_fwd_kv
+    bwd_call = fa.fa_bwd if w.S == w.kv_len else fa.fa_bwd_kv
 
     def step():
-        fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale, stream)
+        fwd_call(qd, kd, vd, out, lse, w.causal, w.scale, stream)
         if w.backward:
-            fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
+            bwd_call(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
 
     def barrier():
         if dist is not None:
@@ -255,10 +279,10 @@ def run_gpu(args, w, rank, world, local_rank):
         barrier()
         for s in range(K):
             ev[s][0].record(stream)
-            fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale, stream)
+            fwd_call(qd, kd, vd, out, lse, w.causal, w.scale, stream)
             ev[s][1].record(stream)
             if w.backward:
-                fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
+                bwd_call(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale, stream)
             ev[s][2].record(stream)
         barrier()
         total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
@@ -312,9 +336,9 @@ def run_gpu(args, w, rank, world, local_rank):
                 stream.wait_event(ev_in[sidx])
                 if started[sidx]:
                     stream.wait_event(ev_out[sidx])        # step k-2's results copied out
-                fa.fa_fwd(iq, ik, iv, oo, ol, w.causal, w.scale, stream)
+                fwd_call(iq, ik, iv, oo, ol, w.causal, w.scale, stream)
                 if w.backward:
-                    fa.fa_bwd(iq, ik, iv, oo, ido, ol, oq, okk, ov, wsd, w.causal, w.scale, stream)
+                    bwd_call(iq, ik, iv, oo, ido, ol, oq, okk, ov, wsd, w.causal, w.scale, stream)
                 ev_comp[sidx].record(stream)
                 with torch.cuda.stream(s_d2h):
                     s_d2h.wait_event(ev_comp[sidx])
@@ -375,30 +399,33 @@ def main():
         w = dataclasses.replace(w, Hq=args.heads, Hkv=args.heads // G)
     peaks, peak_src = load_peaks()
     step_flops = flops(w, True, w.backward)
-    l2_note = (f"inputs larger than L2: Q,K,V,dO = "
-               f"{(fwd_algorithmic_bytes(w) + tensor_bytes(w.B, w.Hq, w.S, w.d, elem_bytes(w))) / 2**20:.0f} MiB "
+    e = elem_bytes(w)
+    in_bytes = 2 * tensor_bytes(w.B, w.Hq, w.S, w.d, e) + 2 * tensor_bytes(w.B, w.Hkv, w.kv_len, w.d, e)
+    l2_note = (f"inputs larger than L2: Q,K,V,dO = {in_bytes / 2**20:.0f} MiB "
                f"read per step vs {L2_BYTES / 2**20:.0f} MiB L2; no flush")
     config = {"workload": w.describe(), "global_batch": w.B * world, "seq_len": w.S,
               "heads": [w.Hq, w.Hkv], "head_dim": w.d, "causal": w.causal,
               "parallelism": f"replicas x{world}", "l2": l2_note}
+    if w.kv_len != w.S:
+        config["kv_len"] = w.kv_len
 
     if args.impl == "reference":
         if rank != 0:
             return
         cores, how = cpu_threads()
-        rows = min(w.S, 2048)
+        block = oracle_block(w, 2048 if w.causal else 512)
         inputs = oracle_inputs(w, min(w.Hq, 4))
         times = []
         for i in range(args.warmup + args.steps):
-            dt, fl = oracle_sample(w, inputs[i % len(inputs)], rows)
+            dt, fl = oracle_sample(w, inputs[i % len(inputs)], block)
             if i >= args.warmup:
                 times.append(dt)
         sec = statistics.mean(times)
         value = fl / sec / 1e12
-        sample = (f"per step: fp64 dense forward + softmax-Jacobian backward of the causal "
-                  f"leading {rows}x{rows} block (rows and keys 0..{rows - 1}) of one query "
-                  f"head of {w.name}, heads 0..{len(inputs) - 1} in turn; {fl / 1e9:.2f} GFLOP "
-                  f"by the causal convention")
+        sample = (f"per step: fp64 dense forward{' + softmax-Jacobian backward' if w.backward else ''} "
+                  f"of the leading block (query rows 0..{block[0] - 1}, keys 0..{block[1] - 1}) "
+                  f"of one query head of {w.name}, heads 0..{len(inputs) - 1} in turn; "
+                  f"{fl / 1e9:.2f} GFLOP by the same convention")
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -453,9 +480,10 @@ def main():
             "algorithmic_bytes": fwd_algorithmic_bytes(w),
         },
         "exp_ceiling": {
-            "exps_per_step": w.B * w.Hq * w.S * (w.S + 1) // 2 if w.causal else w.B * w.Hq * w.S * w.S,
+            "exps_per_step": int(w.B * w.Hq * visible_pairs(w.S, w.kv_len, w.causal)),
             "ex2_per_clk_per_sm": EX2_PER_CLK_SM,
-            "fwd_floor_ms": (w.B * w.Hq * w.S * (w.S + 1) / 2) / (EX2_PER_CLK_SM * 152 * 2.07e9) * 1e3,
+            "fwd_floor_ms": (w.B * w.Hq * visible_pairs(w.S, w.kv_len, w.causal))
+                            / (EX2_PER_CLK_SM * 152 * 2.07e9) * 1e3,
             "note": "forward: one ex2 per visible score; floor at 152 SMs x 2.07 GHz",
         },
         "e2e": {"value": e2e_tf, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
@@ -470,18 +498,20 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         cores, how = cpu_threads()
         total_t, total_f = 0.0, 0
-        rows = min(w.S, 8192)   # the dense oracle holds rows x rows float64 matrices
+        # the dense oracle holds rows x keys float64 matrices
+        block = oracle_block(w, 8192 if w.causal else 4096)
         for hin in oracle_inputs(w, 2):
-            dt, fl = oracle_sample(w, hin, rows)
+            dt, fl = oracle_sample(w, hin, block)
             total_t += dt
             total_f += fl
         line["cpu_baseline"] = {
             "value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores,
             "cores_source": how, "kind": "oracle",
             "sample": f"fp64 dense forward{' + softmax-Jacobian backward' if w.backward else ''} "
-                      f"of the causal leading {rows}x{rows} block of query heads 0 and 1 of "
-                      f"{w.name} (all rows and keys when S = {rows}): "
-                      f"{total_f / 1e9:.1f} GFLOP by the causal convention in {total_t:.2f} s"}
+                      f"of the leading block (query rows 0..{block[0] - 1}, keys 0..{block[1] - 1}) "
+                      f"of query heads 0 and 1 of {w.name} (all of each head when the block "
+                      f"covers it): {total_f / 1e9:.1f} GFLOP by the same convention in "
+                      f"{total_t:.2f} s"}
     if r["dist"] is not None:
         r["dist"].destroy_process_group()
     print(json.dumps(line))

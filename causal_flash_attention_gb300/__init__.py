@@ -2,7 +2,8 @@
 libfa (include/fa.h).
 
 The functions with the C names (`fa_fwd`, `fa_bwd`, `fa_bwd_workspace_bytes`,
-`fa_strerror`, `fa_last_device_status`, `fa_version`) only marshal arguments:
+`fa_fwd_kv`, `fa_bwd_kv`, `fa_bwd_kv_workspace_bytes`, `fa_strerror`,
+`fa_last_device_status`, `fa_version`) only marshal arguments:
 shapes come from the tensors, pointers from `data_ptr()`, and the stream from
 PyTorch's current stream. Every step of the computation runs in libfa's CUDA
 kernels; there is no other code path. `attention_forward` / `attention_backward`
@@ -23,7 +24,8 @@ import torch
 __all__ = [
     "FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_strerror",
     "fa_last_device_status", "fa_version", "attention_forward", "attention_backward",
-    "DTYPE_CODES", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "DTYPE_CODES", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_fwd_kv", "fa_bwd_kv",
+    "fa_bwd_kv_workspace_bytes",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
@@ -53,6 +55,12 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_workspace_bytes.restype = sz
     L.fa_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
     L.fa_bwd.restype = i32
+    L.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp] + [i32] * 7 + [f32, i32, vp]
+    L.fa_fwd_kv.restype = i32
+    L.fa_bwd_kv_workspace_bytes.argtypes = [i32] * 6
+    L.fa_bwd_kv_workspace_bytes.restype = sz
+    L.fa_bwd_kv.argtypes = [vp] * 9 + [i32] * 7 + [f32, i32, vp, sz, vp]
+    L.fa_bwd_kv.restype = i32
     L.fa_strerror.argtypes = [i32]
     L.fa_strerror.restype = ctypes.c_char_p
     L.fa_last_device_status.argtypes = [vp, ctypes.POINTER(i32)]
@@ -84,11 +92,20 @@ def _stream(stream):
 
 
 def _dims(q, k):
+    """(B, Hq, Hkv, S, d) of a self-attention call (q and k of one length)."""
+    B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
+    if Sq != Skv:
+        raise ValueError(f"q has {Sq} rows and k {Skv}: use the *_kv functions")
+    return B, Hq, Hkv, Sq, d
+
+
+def _dims_kv(q, k):
+    """(B, Hq, Hkv, Sq, Skv, d) from q [B,Hq,Sq,d] and k [B,Hkv,Skv,d]."""
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q and k must be [B, H, S, d]")
-    B, Hq, S, d = q.shape
-    Hkv = k.shape[1]
-    return int(B), int(Hq), int(Hkv), int(S), int(d)
+    B, Hq, Sq, d = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    return int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(d)
 
 
 def _check_contig(*ts):
@@ -127,6 +144,38 @@ def fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale=No
         raise FAError(rc, "fa_bwd")
 
 
+def fa_fwd_kv(q, k, v, out, lse, causal=True, scale=None, stream=None):
+    """Call fa_fwd_kv: q/out [B,Hq,Sq,d], k/v [B,Hkv,Skv,d], lse float32 [B,Hq,Sq];
+    the causal mask is aligned to the last key (kv_offset = Skv - Sq)."""
+    _check_contig(q, k, v, out, lse)
+    B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    rc = lib().fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                         d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
+                         _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_fwd_kv")
+
+
+def fa_bwd_kv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d) -> int:
+    return int(lib().fa_bwd_kv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d))
+
+
+def fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale=None,
+              stream=None):
+    """Call fa_bwd_kv (separate query and key/value lengths, as fa_fwd_kv)."""
+    _check_contig(q, k, v, out, dout, lse, dq, dk, dv)
+    B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)), scale,
+                         DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes,
+                         _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_bwd_kv")
+
+
 def fa_last_device_status(stream=None) -> int:
     st = ctypes.c_int(0)
     rc = lib().fa_last_device_status(_stream(stream), ctypes.byref(st))
@@ -136,26 +185,34 @@ def fa_last_device_status(stream=None) -> int:
 
 
 def attention_forward(q, k, v, causal=True, scale=None, stream=None):
-    """Allocate out and lse with PyTorch and run fa_fwd. Returns (out, lse)."""
+    """Allocate out and lse with PyTorch and run fa_fwd (fa_fwd_kv when q and k
+    have different lengths). Returns (out, lse)."""
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, out, lse, causal, scale, stream)
+    if q.shape[2] == k.shape[2]:
+        fa_fwd(q, k, v, out, lse, causal, scale, stream)
+    else:
+        fa_fwd_kv(q, k, v, out, lse, causal, scale, stream)
     return out, lse
 
 
 def workspace_for(q, k):
-    B, Hq, Hkv, S, d = _dims(q, k)
-    n = fa_bwd_workspace_bytes(B, Hq, Hkv, S, d)
+    B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
+    n = fa_bwd_kv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d)
     return torch.empty(n, dtype=torch.uint8, device=q.device)
 
 
 def attention_backward(q, k, v, out, dout, lse, causal=True, scale=None, workspace=None,
                        stream=None):
-    """Allocate dq, dk, dv (and a workspace unless given) and run fa_bwd."""
+    """Allocate dq, dk, dv (and a workspace unless given) and run fa_bwd
+    (fa_bwd_kv when q and k have different lengths)."""
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = workspace_for(q, k)
-    fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    if q.shape[2] == k.shape[2]:
+        fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    else:
+        fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
     return dq, dk, dv
 
 

@@ -61,13 +61,21 @@ bool make_tmap(CUtensorMap* m, const void* base, int BH, int S, int d, bool bf16
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_common(int B, int Hq, int Hkv, int S, int d, float scale, int dtype) {
+// Sq query rows against Skv key/value rows. Under the causal mask query row i
+// stands at position i + (Skv - Sq), so every row sees at least one key only
+// when Skv >= Sq; fewer keys than queries is a shape error.
+int check_common(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, float scale,
+                 int dtype) {
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_SHAPE;
-  // grid and index ranges: B*Hq*ceil(S/256) CTAs, element offsets in 64 bits
+  if (causal && Skv < Sq) return FA_ERR_SHAPE;
+  // grid and index ranges: B*Hq*ceil(Sq/256) forward CTAs, B*Hkv*ceil(Skv/128)
+  // backward CTAs, element offsets in 64 bits
   const long long bh = static_cast<long long>(B) * Hq;
-  if (bh > (1LL << 30) || S > (1 << 30) || bh * ((S + 255) / 256) > 0x7fffffffLL)
+  const long long bhkv = static_cast<long long>(B) * Hkv;
+  if (bh > (1LL << 30) || Sq > (1 << 30) || Skv > (1 << 30) ||
+      bh * ((Sq + 255) / 256) > 0x7fffffffLL || bhkv * ((Skv + 127) / 128) > 0x7fffffffLL)
     return FA_ERR_SHAPE;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_SCALE;
   return FA_OK;
@@ -79,9 +87,9 @@ struct WsLayout {
   size_t dq_acc, delta, lse2, total;
 };
 
-WsLayout ws_layout(int B, int Hq, int S, int d) {
+WsLayout ws_layout(int B, int Hq, int Sq, int d) {
   const long long bh = static_cast<long long>(B) * Hq;
-  const long long s_pad = round_up(S, kTileM);
+  const long long s_pad = round_up(Sq, kTileM);
   WsLayout w;
   w.dq_acc = 0;
   w.delta = static_cast<size_t>(round_up(bh * s_pad * d * 4, 256));
@@ -112,7 +120,8 @@ int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
 const char* fa_strerror(int code) {
   switch (code) {
     case FA_OK: return "ok";
-    case FA_ERR_SHAPE: return "invalid shape (B, Hq, Hkv, S >= 1, Hq % Hkv == 0, d in {64, 128})";
+    case FA_ERR_SHAPE:
+      return "invalid shape (B, Hq, Hkv, S >= 1, Hq % Hkv == 0, d in {64, 128}, causal Skv >= Sq)";
     case FA_ERR_DTYPE: return "unsupported dtype (FA_F32, FA_F16 or FA_BF16)";
     case FA_ERR_NULL: return "a required pointer is NULL";
     case FA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
@@ -126,14 +135,16 @@ const char* fa_strerror(int code) {
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
-           int Hkv, int S, int d, int causal, float scale, int dtype, fa_stream_t stream) {
-  int rc = check_common(B, Hq, Hkv, S, d, scale, dtype);
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+              int Hq, int Hkv, int Sq, int Skv, int d, int causal, float scale, int dtype,
+              fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
   if (rc != FA_OK) return rc;
   if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_ALIGN;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int kv_offset = causal ? Skv - Sq : 0;
 
   if (dtype == FA_F32) {
     SimtParams p{};
@@ -142,7 +153,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
     p.v = static_cast<const float*>(v);
     p.o_out = static_cast<float*>(out);
     p.lse_out = lse;
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.d = d;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.kv_offset = kv_offset; p.d = d;
     p.causal = causal != 0;
     p.scale = scale;
     return launch_fwd_simt(p, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -151,43 +162,55 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
   const bool bf16 = dtype == FA_BF16;
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!make_tmap(&p.tm_q, q, B * Hq, S, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, S, d, bf16) ||
-      !make_tmap(&p.tm_v, v, B * Hkv, S, d, bf16))
+  if (!make_tmap(&p.tm_q, q, B * Hq, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
+      !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16))
     return FA_ERR_TMA;
   p.out = out;
   p.lse = lse;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.kv_offset = kv_offset;
   p.causal = causal != 0;
   p.scale_log2 = scale * kLog2e;
-  p.n_qpairs = (S + 2 * kTileM - 1) / (2 * kTileM);
+  p.n_qpairs = (Sq + 2 * kTileM - 1) / (2 * kTileM);
+  p.kv_tiles_ahead = 1 + (kv_offset + kTileN - 1) / kTileN;
   p.trace = FA_TRACE_PTR;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   return launch_fwd_tc(p, d, bf16, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int S, int d) {
-  if (check_common(B, Hq, Hkv, S, d, 1.f, FA_BF16) != FA_OK) return 0;
-  return ws_layout(B, Hq, S, d).total;
+int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+           int Hkv, int S, int d, int causal, float scale, int dtype, fa_stream_t stream) {
+  return fa_fwd_kv(q, k, v, out, lse, B, Hq, Hkv, S, S, d, causal, scale, dtype, stream);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
-           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int d,
-           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
-           fa_stream_t stream) {
-  int rc = check_common(B, Hq, Hkv, S, d, scale, dtype);
+size_t fa_bwd_kv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d) {
+  // the causal constraint is checked by fa_bwd_kv itself
+  if (check_common(B, Hq, Hkv, Sq, Skv, d, 0, 1.f, FA_BF16) != FA_OK) return 0;
+  return ws_layout(B, Hq, Sq, d).total;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int S, int d) {
+  return fa_bwd_kv_workspace_bytes(B, Hq, Hkv, S, S, d);
+}
+
+int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+              int Skv, int d, int causal, float scale, int dtype, void* workspace,
+              size_t workspace_bytes, fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
   if (rc != FA_OK) return rc;
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
       !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_ALIGN;
-  const WsLayout ws = ws_layout(B, Hq, S, d);
+  const WsLayout ws = ws_layout(B, Hq, Sq, d);
   if (!workspace || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   const int BH = B * Hq;
-  const int S_pad = static_cast<int>(round_up(S, kTileM));
+  const int Sq_pad = static_cast<int>(round_up(Sq, kTileM));
+  const int kv_offset = causal ? Skv - Sq : 0;
 
   BwdPreParams pre;
   pre.out = out;
@@ -196,7 +219,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out, const v
   pre.delta = reinterpret_cast<float*>(wsb + ws.delta);
   pre.lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
   pre.dq_acc = dtype == FA_F32 ? nullptr : reinterpret_cast<float*>(wsb + ws.dq_acc);
-  pre.BH = BH; pre.S = S; pre.S_pad = S_pad; pre.d = d;
+  pre.BH = BH; pre.Sq = Sq; pre.Sq_pad = Sq_pad; pre.d = d;
   pre.dtype = dtype;
   if (launch_bwd_pre(pre, st) != cudaSuccess) return FA_ERR_CUDA;
 
@@ -211,7 +234,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out, const v
     p.dq = static_cast<float*>(dq);
     p.dk = static_cast<float*>(dk);
     p.dv = static_cast<float*>(dv);
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.d = d;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.kv_offset = kv_offset; p.d = d;
     p.causal = causal != 0;
     p.scale = scale;
     return launch_bwd_simt(p, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -220,19 +243,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out, const v
   const bool bf16 = dtype == FA_BF16;
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!make_tmap(&p.tm_q, q, BH, S, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, S, d, bf16) ||
-      !make_tmap(&p.tm_v, v, B * Hkv, S, d, bf16) || !make_tmap(&p.tm_do, dout, BH, S, d, bf16))
+  if (!make_tmap(&p.tm_q, q, BH, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
+      !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16))
     return FA_ERR_TMA;
   p.delta = pre.delta;
   p.lse2 = pre.lse2;
   p.dq_acc = pre.dq_acc;
   p.dk = dk;
   p.dv = dv;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.S_pad = S_pad;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.Sq_pad = Sq_pad;
+  p.kv_offset = kv_offset;
   p.causal = causal != 0;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
-  p.n_kv_tiles = (S + kTileN - 1) / kTileN;
+  p.n_kv_tiles = (Skv + kTileN - 1) / kTileN;
+  p.n_q_tiles = (Sq + kTileM - 1) / kTileM;
   p.trace = FA_TRACE_PTR;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
@@ -241,10 +266,18 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out, const v
   DqConvertParams cv;
   cv.dq_acc = pre.dq_acc;
   cv.dq = dq;
-  cv.BH = BH; cv.S = S; cv.S_pad = S_pad; cv.d = d;
+  cv.BH = BH; cv.Sq = Sq; cv.Sq_pad = Sq_pad; cv.d = d;
   cv.scale = scale;
   cv.dtype = dtype;
   return launch_dq_convert(cv, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S, int d,
+           int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream) {
+  return fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, S, S, d, causal, scale, dtype,
+                   workspace, workspace_bytes, stream);
 }
 
 int fa_last_device_status(fa_stream_t stream, int* status) {

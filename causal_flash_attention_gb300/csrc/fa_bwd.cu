@@ -12,8 +12,10 @@
 //   2. bwd_main:   one CTA per (batch, key/value head, 128-row key tile j). K_j and
 //                  V_j stay in shared memory, dK_j and dV_j stay in tensor memory
 //                  for the whole CTA (so no atomics for them), and the CTA walks
-//                  every query tile i >= j (causal) of every query head of the
-//                  group. Per step, on the tensor cores:
+//                  every query tile that can see a key of tile j (causal: rows
+//                  at positions i + kv_offset >= the tile's first key, with
+//                  kv_offset = Skv - Sq) of every query head of the group.
+//                  Per step, on the tensor cores:
 //                    S^T  = K_j Q_i^T          -> TMEM (kv rows x q cols)
 //                    dP^T = V_j dO_i^T         -> TMEM
 //                    [softmax warps: P^T = 2^(S^T*c - L*log2e), masked; written as
@@ -85,17 +87,17 @@ template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ------------------------------------------------------------------ pre --
-// One warp per (head row, sequence row) in [0, S_pad): D = <dO, O> in fp32,
+// One warp per (head row, query row) in [0, Sq_pad): D = <dO, O> in fp32,
 // L*log2(e), and a zeroed dQ accumulator row.
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // bh * S_pad + i
-  if (row >= static_cast<long long>(p.BH) * p.S_pad) return;
-  const int bh = static_cast<int>(row / p.S_pad), i = static_cast<int>(row % p.S_pad);
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // bh * Sq_pad + i
+  if (row >= static_cast<long long>(p.BH) * p.Sq_pad) return;
+  const int bh = static_cast<int>(row / p.Sq_pad), i = static_cast<int>(row % p.Sq_pad);
   float dsum = 0.f;
-  if (i < p.S) {
-    const size_t off = (static_cast<size_t>(bh) * p.S + i) * p.d;
+  if (i < p.Sq) {
+    const size_t off = (static_cast<size_t>(bh) * p.Sq + i) * p.d;
     const T* o = static_cast<const T*>(p.out) + off;
     const T* g = static_cast<const T*>(p.dout) + off;
     for (int e = lane; e < p.d; e += 32) dsum = fmaf(to_f(o[e]), to_f(g[e]), dsum);
@@ -103,8 +105,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
   if (lane == 0) {
-    p.delta[row] = (i < p.S) ? dsum : 0.f;
-    p.lse2[row] = (i < p.S) ? p.lse[static_cast<size_t>(bh) * p.S + i] * kLog2eF : INFINITY;
+    p.delta[row] = (i < p.Sq) ? dsum : 0.f;
+    p.lse2[row] = (i < p.Sq) ? p.lse[static_cast<size_t>(bh) * p.Sq + i] * kLog2eF : INFINITY;
   }
   if (p.dq_acc) {
     float4* acc = reinterpret_cast<float4*>(p.dq_acc + static_cast<size_t>(row) * p.d);
@@ -113,18 +115,18 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 }
 
 // -------------------------------------------------------------- convert --
-// dq = scale * dq_acc (rows < S), 8 elements per thread.
+// dq = scale * dq_acc (rows < Sq), 8 elements per thread.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
-  const long long n8 = static_cast<long long>(p.BH) * p.S * p.d / 8;
+  const long long n8 = static_cast<long long>(p.BH) * p.Sq * p.d / 8;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long e = t * 8;
-    const long long rowd = e / p.d;                      // bh * S + i
+    const long long rowd = e / p.d;                      // bh * Sq + i
     const int col = static_cast<int>(e % p.d);
-    const long long bh = rowd / p.S, i = rowd % p.S;
+    const long long bh = rowd / p.Sq, i = rowd % p.Sq;
     const float4* src =
-        reinterpret_cast<const float4*>(p.dq_acc + (bh * p.S_pad + i) * p.d + col);
+        reinterpret_cast<const float4*>(p.dq_acc + (bh * p.Sq_pad + i) * p.d + col);
     const float4 a = src[0], b = src[1];
     uint4 w;
     w.x = pack2<kBf16>(a.x * p.scale, a.y * p.scale);
@@ -180,8 +182,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bkv = static_cast<int>(blockIdx.x) % BHkv;
   const int b = bkv / p.Hkv, g = bkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
-  const int n_qt = p.n_kv_tiles;                 // query tiles per head (same S)
-  const int i_start = p.causal ? j : 0;
+  const int n_qt = p.n_q_tiles;                  // query tiles per head
+  // causal: the first query tile holding a row at position >= this tile's
+  // first key (query row i stands at position i + kv_offset)
+  const int i_start = p.causal ? max(0, j * kTileN - p.kv_offset) / kTileM : 0;
   const int n_i = n_qt - i_start;
   const int n_iter = G * n_i;
   auto bh_of = [&](int it) { return b * p.Hq + g * G + it / n_i; };
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sbase + Cfg::kOffDO + st * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_do,
                       fb, c * kChunk, i * kTileM, bh);
         }
-        const size_t roff = static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM;
+        const size_t roff = static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM;
         bulk_load(sbase + Cfg::kOffRow + st * 1024, p.lse2 + roff, 512, fb);
         bulk_load(sbase + Cfg::kOffRow + st * 1024 + 512, p.delta + roff, 512, fb);
         tr(40);
@@ -383,10 +387,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tr(20);
       tc_fence_after();
       // Masked entries: key past the sequence end, or (causal) key after the
-      // query. Column qc of this row is masked iff qc < thr; thr <= 0 on every
-      // tile that is neither diagonal nor ragged, which skip the selects.
+      // query's position q + kv_offset. Column qc of this row is masked iff
+      // qc < thr; thr <= 0 on every tile that is neither diagonal nor ragged,
+      // which skip the selects.
       const int q0 = i * kTileM;
-      const int thr = kv >= p.S ? kTileM : (p.causal ? min(kv - q0, kTileM) : 0);
+      const int thr = kv >= p.Skv ? kTileM : (p.causal ? min(kv - p.kv_offset - q0, kTileM) : 0);
       const bool any_mask = __any_sync(0xffffffffu, thr > 0);
       uint32_t ppk[64];
 #pragma unroll
@@ -457,13 +462,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       tc_fence_after();
       using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      Elem* dst = reinterpret_cast<Elem*>(p.dk) + (static_cast<size_t>(bkv) * p.S + kv) * D;
+      Elem* dst = reinterpret_cast<Elem*>(p.dk) + (static_cast<size_t>(bkv) * p.Skv + kv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_off + cc * 32, o);
         tmem_wait_ld();
-        if (kv < p.S) {
+        if (kv < p.Skv) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -501,7 +506,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(dq_empty);
       tr(31);
       const int bh = bh_of(it), i = i_of(it);
-      float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.S_pad + static_cast<size_t>(i) * kTileM) * D;
+      float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM) * D;
       if constexpr (kDqT) {
         // warp-wide: 32 consecutive head-dimension entries of one query row
         float* col = tile + r;
@@ -522,13 +527,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int kv = j * kTileN + r;
       using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      Elem* dst = reinterpret_cast<Elem*>(p.dv) + (static_cast<size_t>(bkv) * p.S + kv) * D;
+      Elem* dst = reinterpret_cast<Elem*>(p.dv) + (static_cast<size_t>(bkv) * p.Skv + kv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_off + 128 + cc * 32, o);
         tmem_wait_ld();
-        if (kv < p.S) {
+        if (kv < p.Skv) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -563,7 +568,7 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.BH) * p.S_pad;
+  const long long rows = static_cast<long long>(p.BH) * p.Sq_pad;
   const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
   if (p.dtype == 0) bwd_pre_kernel<float><<<grid, 256, 0, stream>>>(p);
   else if (p.dtype == 1) bwd_pre_kernel<__half><<<grid, 256, 0, stream>>>(p);
@@ -577,7 +582,7 @@ cudaError_t launch_bwd_tc(const BwdParams& p, int d, bool bf16, cudaStream_t str
 }
 
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
-  const long long n8 = static_cast<long long>(p.BH) * p.S * p.d / 8;
+  const long long n8 = static_cast<long long>(p.BH) * p.Sq * p.d / 8;
   const unsigned grid = static_cast<unsigned>(std::min<long long>((n8 + 255) / 256, 152LL * 16));
   if (p.dtype == 2) dq_convert_kernel<true><<<grid, 256, 0, stream>>>(p);
   else dq_convert_kernel<false><<<grid, 256, 0, stream>>>(p);

@@ -10,8 +10,10 @@
 //
 // One CTA owns two 128-row query tiles of one (batch, query head) and walks
 // the key/value tiles up to the causal diagonal (tiles wholly above it are
-// never loaded; "Phase 14", section Causal Mask, tile-level skip). Key/value
-// head = query head / (Hq / Hkv) ("Phase 14", section GQA 支持).
+// never loaded; "Phase 14", section Causal Mask, tile-level skip). With Sq
+// queries against Skv >= Sq keys, query row i stands at position
+// i + (Skv - Sq), the kv_offset of the same section. Key/value head = query
+// head / (Hq / Hkv) ("Phase 14", section GQA 支持).
 //
 // Warp roles (320 threads):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles into two
@@ -122,13 +124,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int bh = static_cast<int>(blockIdx.x) % BHq;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
-  const int n_kv_total = (p.S + kTileN - 1) / kTileN;
+  // key/value tiles each query tile walks (0 past the sequence end). Causal:
+  // query tile qt's rows end below q_end = min(128 (qt + 1), Sq) and see keys
+  // below q_end + kv_offset <= Skv, i.e. tiles up to qt + kv_tiles_ahead for a
+  // full tile and every tile for the last, ragged one.
+  const int n_kv_total = (p.Skv + kTileN - 1) / kTileN;
   int n_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int q0 = pair * 2 * kTileM + t * kTileM;
-    if (q0 >= p.S) n_t[t] = 0;
-    else n_t[t] = p.causal ? min(q0 / kTileN + 1, n_kv_total) : n_kv_total;
+    if (q0 >= p.Sq) n_t[t] = 0;
+    else n_t[t] = p.causal ? min(q0 / kTileN + p.kv_tiles_ahead, n_kv_total) : n_kv_total;
   }
   const int n_load = max(n_t[0], n_t[1]);
 
@@ -299,8 +305,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int i = 0; i < kTileN; ++i) s[i] = __uint_as_float(raw[i]);
       }
       const int kv0 = j * kTileN;
-      // inline mask: causal (key > query) and keys past the sequence end
-      const int lim = p.causal ? min(row, p.S - 1) : p.S - 1;   // last visible key
+      // inline mask: causal (key after the query's position) and keys past the
+      // sequence end; lim = last visible key of this row (rows past Sq are
+      // never stored, so their limit may run past Skv - 1)
+      const int lim = p.causal ? row + p.kv_offset : p.Skv - 1;
       if (kv0 + kTileN - 1 > lim) {
 #pragma unroll
         for (int i = 0; i < kTileN; ++i)
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         const float inv_l = 1.f / l;
         using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-        Elem* orow = reinterpret_cast<Elem*>(p.out) + (static_cast<size_t>(bh) * p.S + row) * D;
+        Elem* orow = reinterpret_cast<Elem*>(p.out) + (static_cast<size_t>(bh) * p.Sq + row) * D;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -379,15 +387,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 0; i < 16; ++i)
             w[i] = pack2<kBf16>(__uint_as_float(o[2 * i]) * inv_l,
                                 __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (row < p.S) {
+          if (row < p.Sq) {
             uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
         }
-        if (row < p.S)
-          p.lse[static_cast<size_t>(bh) * p.S + row] = (m_ref + __log2f(l)) * kLn2;
+        if (row < p.Sq)
+          p.lse[static_cast<size_t>(bh) * p.Sq + row] = (m_ref + __log2f(l)) * kLn2;
       }
     }
   }

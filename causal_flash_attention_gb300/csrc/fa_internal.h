@@ -15,54 +15,60 @@ constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 constexpr int kChunk = 64;
 
+// Sequence lengths: Sq query rows, Skv key/value rows (equal for
+// self-attention). Under the causal mask query row i stands at position
+// i + kv_offset, kv_offset = Skv - Sq >= 0 (0 without the mask).
 struct FwdParams {
-  CUtensorMap tm_q;   // [B*Hq][S][d], box (64, 128, 1), 128B swizzle
-  CUtensorMap tm_k;   // [B*Hkv][S][d]
-  CUtensorMap tm_v;   // [B*Hkv][S][d]
-  void* out;          // [B*Hq][S][d], same dtype as q
-  float* lse;         // [B*Hq][S], natural log
-  int B, Hq, Hkv, S;
+  CUtensorMap tm_q;   // [B*Hq][Sq][d], box (64, 128, 1), 128B swizzle
+  CUtensorMap tm_k;   // [B*Hkv][Skv][d]
+  CUtensorMap tm_v;   // [B*Hkv][Skv][d]
+  void* out;          // [B*Hq][Sq][d], same dtype as q
+  float* lse;         // [B*Hq][Sq], natural log
+  int B, Hq, Hkv, Sq, Skv, kv_offset;
   int causal;
   float scale_log2;   // softmax scale * log2(e)
-  int n_qpairs;       // ceil(S / 256): CTAs per (batch, query head)
+  int n_qpairs;       // ceil(Sq / 256): CTAs per (batch, query head)
+  int kv_tiles_ahead; // 1 + ceil(kv_offset / 128): key tiles a full causal
+                      // query tile qt walks is qt + kv_tiles_ahead
   int* status;        // device status word (wait timeouts)
   unsigned long long* trace;   // timeline buffer of trace builds (FA_TRACE); else null
 };
 
 struct BwdPreParams {
-  const void* out;    // [B*Hq][S][d]
-  const void* dout;   // [B*Hq][S][d]
-  const float* lse;   // [B*Hq][S]
-  float* delta;       // [B*Hq][S_pad]   D_i = <dO_i, O_i>, 0 on padding rows
-  float* lse2;        // [B*Hq][S_pad]   LSE_i * log2(e), +inf on padding rows
-  float* dq_acc;      // [B*Hq][S_pad][d] fp32, zeroed here
-  int BH, S, S_pad, d;
+  const void* out;    // [B*Hq][Sq][d]
+  const void* dout;   // [B*Hq][Sq][d]
+  const float* lse;   // [B*Hq][Sq]
+  float* delta;       // [B*Hq][Sq_pad]   D_i = <dO_i, O_i>, 0 on padding rows
+  float* lse2;        // [B*Hq][Sq_pad]   LSE_i * log2(e), +inf on padding rows
+  float* dq_acc;      // [B*Hq][Sq_pad][d] fp32, zeroed here
+  int BH, Sq, Sq_pad, d;
   int dtype;
 };
 
 struct BwdParams {
-  CUtensorMap tm_q;   // [B*Hq][S][d]
-  CUtensorMap tm_k;   // [B*Hkv][S][d]
-  CUtensorMap tm_v;   // [B*Hkv][S][d]
-  CUtensorMap tm_do;  // [B*Hq][S][d]
-  const float* delta; // [B*Hq][S_pad]
-  const float* lse2;  // [B*Hq][S_pad]
-  float* dq_acc;      // [B*Hq][S_pad][d]
-  void* dk;           // [B*Hkv][S][d]
-  void* dv;           // [B*Hkv][S][d]
-  int B, Hq, Hkv, S, S_pad;
+  CUtensorMap tm_q;   // [B*Hq][Sq][d]
+  CUtensorMap tm_k;   // [B*Hkv][Skv][d]
+  CUtensorMap tm_v;   // [B*Hkv][Skv][d]
+  CUtensorMap tm_do;  // [B*Hq][Sq][d]
+  const float* delta; // [B*Hq][Sq_pad]
+  const float* lse2;  // [B*Hq][Sq_pad]
+  float* dq_acc;      // [B*Hq][Sq_pad][d]
+  void* dk;           // [B*Hkv][Skv][d]
+  void* dv;           // [B*Hkv][Skv][d]
+  int B, Hq, Hkv, Sq, Skv, Sq_pad, kv_offset;
   int causal;
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
-  int n_kv_tiles;     // ceil(S / 128)
+  int n_kv_tiles;     // ceil(Skv / 128): CTAs per (batch, key/value head)
+  int n_q_tiles;      // ceil(Sq / 128)
   int* status;
   unsigned long long* trace;   // timeline buffer of trace builds (FA_TRACE); else null
 };
 
 struct DqConvertParams {
-  const float* dq_acc;  // [B*Hq][S_pad][d]
-  void* dq;             // [B*Hq][S][d]
-  int BH, S, S_pad, d;
+  const float* dq_acc;  // [B*Hq][Sq_pad][d]
+  void* dq;             // [B*Hq][Sq][d]
+  int BH, Sq, Sq_pad, d;
   float scale;
   int dtype;
 };
@@ -71,8 +77,8 @@ struct DqConvertParams {
 struct SimtParams {
   const float *q, *k, *v, *out, *dout, *lse;
   float *o_out, *lse_out, *dq, *dk, *dv;
-  const float* delta;
-  int B, Hq, Hkv, S, d;
+  const float* delta;   // [B*Hq][Sq_pad]
+  int B, Hq, Hkv, Sq, Skv, kv_offset, d;
   int causal;
   float scale;
 };

@@ -42,13 +42,13 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt(const SimtParams p) {
   const int d = p.d, per = d / 32;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int g = h / (p.Hq / p.Hkv);
-  const float* qrow = p.q + (static_cast<size_t>(bh) * p.S + (i < p.S ? i : 0)) * d;
+  const float* qrow = p.q + (static_cast<size_t>(bh) * p.Sq + (i < p.Sq ? i : 0)) * d;
   for (int e = lane; e < d; e += 32) qs[warp][e] = qrow[e];
   __syncwarp();
-  if (i >= p.S) return;
-  const float* kh = p.k + static_cast<size_t>(b * p.Hkv + g) * p.S * d;
-  const float* vh = p.v + static_cast<size_t>(b * p.Hkv + g) * p.S * d;
-  const int n = p.causal ? i + 1 : p.S;
+  if (i >= p.Sq) return;
+  const float* kh = p.k + static_cast<size_t>(b * p.Hkv + g) * p.Skv * d;
+  const float* vh = p.v + static_cast<size_t>(b * p.Hkv + g) * p.Skv * d;
+  const int n = p.causal ? i + 1 + p.kv_offset : p.Skv;   // visible keys
   float m = -INFINITY, l = 0.f, acc[kMaxPer] = {0.f, 0.f, 0.f, 0.f};
   for (int j0 = 0; j0 < n; j0 += 32) {
     const int j = j0 + lane;
@@ -66,33 +66,33 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt(const SimtParams p) {
     }
     m = m_new;
   }
-  float* orow = p.o_out + (static_cast<size_t>(bh) * p.S + i) * d;
+  float* orow = p.o_out + (static_cast<size_t>(bh) * p.Sq + i) * d;
   for (int u = 0; u < per; ++u) orow[lane + 32 * u] = acc[u] / l;
-  if (lane == 0) p.lse_out[static_cast<size_t>(bh) * p.S + i] = m + logf(l);
+  if (lane == 0) p.lse_out[static_cast<size_t>(bh) * p.Sq + i] = m + logf(l);
 }
 
 // dQ_i = scale * sum_j p_ij (dp_ij - D_i) K_j, one warp per query row.
-__global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt(const SimtParams p, int S_pad) {
+__global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt(const SimtParams p, int Sq_pad) {
   __shared__ float qs[kWarps][128], dos[kWarps][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
   const int i = blockIdx.x * kWarps + warp;
   const int d = p.d, per = d / 32;
-  const int ii = i < p.S ? i : 0;
-  const size_t rowoff = (static_cast<size_t>(bh) * p.S + ii) * d;
+  const int ii = i < p.Sq ? i : 0;
+  const size_t rowoff = (static_cast<size_t>(bh) * p.Sq + ii) * d;
   for (int e = lane; e < d; e += 32) {
     qs[warp][e] = p.q[rowoff + e];
     dos[warp][e] = p.dout[rowoff + e];
   }
   __syncwarp();
-  if (i >= p.S) return;
+  if (i >= p.Sq) return;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int g = h / (p.Hq / p.Hkv);
-  const float* kh = p.k + static_cast<size_t>(b * p.Hkv + g) * p.S * d;
-  const float* vh = p.v + static_cast<size_t>(b * p.Hkv + g) * p.S * d;
-  const float L = p.lse[static_cast<size_t>(bh) * p.S + i];
-  const float Di = p.delta[static_cast<size_t>(bh) * S_pad + i];
-  const int n = p.causal ? i + 1 : p.S;
+  const float* kh = p.k + static_cast<size_t>(b * p.Hkv + g) * p.Skv * d;
+  const float* vh = p.v + static_cast<size_t>(b * p.Hkv + g) * p.Skv * d;
+  const float L = p.lse[static_cast<size_t>(bh) * p.Sq + i];
+  const float Di = p.delta[static_cast<size_t>(bh) * Sq_pad + i];
+  const int n = p.causal ? i + 1 + p.kv_offset : p.Skv;
   float acc[kMaxPer] = {0.f, 0.f, 0.f, 0.f};
   for (int j0 = 0; j0 < n; j0 += 32) {
     const int j = j0 + lane;
@@ -110,44 +110,45 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt(const SimtParams p, i
       for (int u = 0; u < per; ++u) acc[u] = fmaf(dst, kr[lane + 32 * u], acc[u]);
     }
   }
-  float* out = p.dq + (static_cast<size_t>(bh) * p.S + i) * d;
+  float* out = p.dq + (static_cast<size_t>(bh) * p.Sq + i) * d;
   for (int u = 0; u < per; ++u) out[lane + 32 * u] = p.scale * acc[u];
 }
 
 // dK_j = scale * sum_{h in group, i} ds_ij Q_i and dV_j = sum p_ij dO_i, one
 // warp per key row.
-__global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt(const SimtParams p, int S_pad) {
+__global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt(const SimtParams p, int Sq_pad) {
   __shared__ float ks[kWarps][128], vs[kWarps][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bkv = blockIdx.y;   // b * Hkv + g
   const int j = blockIdx.x * kWarps + warp;
   const int d = p.d, per = d / 32;
-  const int jj = j < p.S ? j : 0;
-  const size_t rowoff = (static_cast<size_t>(bkv) * p.S + jj) * d;
+  const int jj = j < p.Skv ? j : 0;
+  const size_t rowoff = (static_cast<size_t>(bkv) * p.Skv + jj) * d;
   for (int e = lane; e < d; e += 32) {
     ks[warp][e] = p.k[rowoff + e];
     vs[warp][e] = p.v[rowoff + e];
   }
   __syncwarp();
-  if (j >= p.S) return;
+  if (j >= p.Skv) return;
   const int b = bkv / p.Hkv, g = bkv % p.Hkv;
   const int G = p.Hq / p.Hkv;
   float dk[kMaxPer] = {0.f, 0.f, 0.f, 0.f}, dv[kMaxPer] = {0.f, 0.f, 0.f, 0.f};
   for (int h = g * G; h < (g + 1) * G; ++h) {
     const int bh = b * p.Hq + h;
-    const float* qh = p.q + static_cast<size_t>(bh) * p.S * d;
-    const float* doh = p.dout + static_cast<size_t>(bh) * p.S * d;
-    const int i_start = p.causal ? j : 0;
-    for (int i0 = i_start; i0 < p.S; i0 += 32) {
+    const float* qh = p.q + static_cast<size_t>(bh) * p.Sq * d;
+    const float* doh = p.dout + static_cast<size_t>(bh) * p.Sq * d;
+    // causal: query rows at positions i + kv_offset >= j see key j
+    const int i_start = p.causal ? max(0, j - p.kv_offset) : 0;
+    for (int i0 = i_start; i0 < p.Sq; i0 += 32) {
       const int i = i0 + lane;
       float pij = 0.f, ds = 0.f;
-      if (i < p.S) {
+      if (i < p.Sq) {
         const float s = p.scale * dot_row(qh + static_cast<size_t>(i) * d, ks[warp], d);
-        pij = expf(s - p.lse[static_cast<size_t>(bh) * p.S + i]);
+        pij = expf(s - p.lse[static_cast<size_t>(bh) * p.Sq + i]);
         const float dp = dot_row(doh + static_cast<size_t>(i) * d, vs[warp], d);
-        ds = pij * (dp - p.delta[static_cast<size_t>(bh) * S_pad + i]);
+        ds = pij * (dp - p.delta[static_cast<size_t>(bh) * Sq_pad + i]);
       }
-      const int cnt = min(32, p.S - i0);
+      const int cnt = min(32, p.Sq - i0);
       for (int t = 0; t < cnt; ++t) {
         const float pt = __shfl_sync(0xffffffffu, pij, t);
         const float dt = __shfl_sync(0xffffffffu, ds, t);
@@ -171,19 +172,19 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt(const SimtParams p,
 }  // namespace
 
 cudaError_t launch_fwd_simt(const SimtParams& p, cudaStream_t stream) {
-  dim3 grid((p.S + kWarps - 1) / kWarps, p.B * p.Hq);
+  dim3 grid((p.Sq + kWarps - 1) / kWarps, p.B * p.Hq);
   fwd_simt<<<grid, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_simt(const SimtParams& p, cudaStream_t stream) {
-  const int S_pad = (p.S + kTileM - 1) / kTileM * kTileM;
-  dim3 g1((p.S + kWarps - 1) / kWarps, p.B * p.Hq);
-  bwd_dq_simt<<<g1, kWarps * 32, 0, stream>>>(p, S_pad);
+  const int Sq_pad = (p.Sq + kTileM - 1) / kTileM * kTileM;
+  dim3 g1((p.Sq + kWarps - 1) / kWarps, p.B * p.Hq);
+  bwd_dq_simt<<<g1, kWarps * 32, 0, stream>>>(p, Sq_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 g2((p.S + kWarps - 1) / kWarps, p.B * p.Hkv);
-  bwd_dkdv_simt<<<g2, kWarps * 32, 0, stream>>>(p, S_pad);
+  dim3 g2((p.Skv + kWarps - 1) / kWarps, p.B * p.Hkv);
+  bwd_dkdv_simt<<<g2, kWarps * 32, 0, stream>>>(p, Sq_pad);
   return cudaGetLastError();
 }
 

@@ -63,7 +63,8 @@ typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
 
 enum {
   FA_OK = 0,
-  FA_ERR_SHAPE = -1,        /* B, Hq, Hkv, S < 1, Hq % Hkv != 0, d not 64/128, or too large */
+  FA_ERR_SHAPE = -1,        /* B, Hq, Hkv, S < 1, Hq % Hkv != 0, d not 64/128, causal with
+                               Skv < Sq (fa_*_kv), or too large */
   FA_ERR_DTYPE = -2,        /* dtype not one of fa_dtype */
   FA_ERR_NULL = -3,         /* a required pointer is NULL */
   FA_ERR_ALIGN = -4,        /* a pointer is not 16-byte aligned */
@@ -103,6 +104,36 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out,
            int B, int Hq, int Hkv, int S, int d, int causal, float scale,
            int dtype, void* workspace, size_t workspace_bytes,
            fa_stream_t stream);
+
+/*
+ * Separate query and key/value lengths: Sq query rows against Skv key/value
+ * rows, for a chunk of queries at the end of a longer context (chunked
+ * prefill, a few new tokens against a KV cache) or, without the mask, any two
+ * lengths. Layout:
+ *   q, out, dout, dq : [B][Hq][Sq][d]     k, v, dk, dv : [B][Hkv][Skv][d]
+ *   lse              : [B][Hq][Sq]  float32
+ * With causal != 0, query row i stands at sequence position i + kv_offset,
+ * kv_offset = Skv - Sq, and key j is masked when j > i + kv_offset ("Phase 14:
+ * Flash Attention 2 for SM120", section Causal Mask: kv_offset = kv_len -
+ * q_len, for a KV cache longer than Q). Causal calls need Skv >= Sq, else
+ * FA_ERR_SHAPE (rows with no visible key have no softmax). Everything else
+ * (dtypes, d, alignment, ownership, errors, asynchrony) is as for fa_fwd and
+ * fa_bwd, which are these calls with Sq = Skv = S.
+ */
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* out, float* lse,
+              int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+              float scale, int dtype, fa_stream_t stream);
+
+/* Workspace bytes of fa_bwd_kv: as fa_bwd_workspace_bytes, sized by Sq (the
+ * dQ accumulator and the per-row D and LSE have one row per query). Returns 0
+ * for invalid sizes. */
+size_t fa_bwd_kv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d);
+
+int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out,
+              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+              int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+              float scale, int dtype, void* workspace, size_t workspace_bytes,
+              fa_stream_t stream);
 
 /*
  * Size of the fixed device scratch array behind fa_bwd_noalloc (32 MiB). A

@@ -20,3 +20,12 @@ def fa_lib():
     import causal_flash_attention_gb300 as fa
     fa.lib()
     return fa
+
+
+@pytest.fixture(scope="module")
+def fa(fa_lib):
+    """The binding on a CUDA device; skips where there is none."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return fa_lib

@@ -108,3 +108,52 @@ def test_package_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         fa.lib()
+
+
+# separate query / key-value lengths (fa_fwd_kv, fa_bwd_kv)
+def _fwd_kv(L, q=16, k=16, v=16, out=16, lse=16, B=1, Hq=2, Hkv=1, Sq=128, Skv=300, d=64,
+            causal=1, scale=0.125, dtype=2):
+    return L.fa_fwd_kv(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Sq=301, Skv=300), FA_ERR_SHAPE),              # causal: fewer keys than queries
+    (dict(Sq=301, Skv=300, causal=0, q=None), FA_ERR_NULL),   # unmasked: any lengths
+    (dict(Sq=0), FA_ERR_SHAPE), (dict(Skv=0), FA_ERR_SHAPE), (dict(Skv=-5), FA_ERR_SHAPE),
+    (dict(d=80), FA_ERR_SHAPE), (dict(dtype=5), FA_ERR_DTYPE), (dict(scale=0.0), FA_ERR_SCALE),
+    (dict(v=None), FA_ERR_NULL), (dict(k=8), FA_ERR_ALIGN), (dict(out=40), FA_ERR_ALIGN),
+    (dict(Sq=1, Skv=(1 << 31) - 1), FA_ERR_SHAPE),
+])
+def test_fwd_kv_rejects_bad_arguments(fa_lib, kw, code):
+    assert _fwd_kv(fa_lib.lib(), **kw) == code
+
+
+def _bwd_kv(L, ptr=256, B=1, Hq=2, Hkv=1, Sq=128, Skv=300, d=64, causal=1, scale=0.125,
+            dtype=2, ws=256, ws_bytes=1 << 30, **over):
+    ptrs = dict(q=ptr, k=ptr, v=ptr, out=ptr, dout=ptr, lse=ptr, dq=ptr, dk=ptr, dv=ptr)
+    ptrs.update(over)
+    return L.fa_bwd_kv(ptrs["q"], ptrs["k"], ptrs["v"], ptrs["out"], ptrs["dout"], ptrs["lse"],
+                       ptrs["dq"], ptrs["dk"], ptrs["dv"], B, Hq, Hkv, Sq, Skv, d, causal, scale,
+                       dtype, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Sq=400, Skv=300), FA_ERR_SHAPE), (dict(Sq=400, Skv=300, causal=0, dk=None), FA_ERR_NULL),
+    (dict(Skv=0), FA_ERR_SHAPE), (dict(dk=None), FA_ERR_NULL), (dict(dv=24), FA_ERR_ALIGN),
+    (dict(ws=None), FA_ERR_WORKSPACE), (dict(ws_bytes=1024), FA_ERR_WORKSPACE),
+    (dict(ws=16 + 256), FA_ERR_ALIGN),
+])
+def test_bwd_kv_rejects_bad_arguments(fa_lib, kw, code):
+    assert _bwd_kv(fa_lib.lib(), **kw) == code
+
+
+def test_kv_workspace_is_sized_by_the_query_length(fa_lib):
+    up = lambda x, m: (x + m - 1) // m * m
+    for B, Hq, Hkv, Sq, Skv, d in [(1, 32, 8, 2048, 8192, 128), (2, 4, 2, 1, 777, 64),
+                                   (1, 2, 2, 300, 129, 128)]:
+        bh, sp = B * Hq, up(Sq, 128)
+        want = up(bh * sp * d * 4, 256) + 2 * up(bh * sp * 4, 256)
+        assert fa_lib.fa_bwd_kv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d) == want
+    assert fa_lib.fa_bwd_kv_workspace_bytes(1, 2, 2, 128, 0, 64) == 0
+    assert fa_lib.fa_bwd_kv_workspace_bytes(1, 2, 2, 128, 128, 64) == \
+        fa_lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 64)

@@ -1,7 +1,7 @@
 """GPU parity: libfa's CUDA kernels (through the C ABI) against the fp64 oracle
 on the same seeded inputs.
 
-Bars (from the task's stated tolerances): forward max|out - out_oracle| <= 1e-2
+Bars: forward max|out - out_oracle| <= 1e-2
 and max|lse - lse_oracle| <= 2e-3; backward max|dX - dX_oracle| <=
 2e-2 * max(max|dX_oracle|, 1e-3) for X in {Q, K, V}, per tensor (the 1e-3
 floor only matters where the oracle's gradient is exactly zero, e.g. dQ and dK
@@ -25,47 +25,8 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-OUT_TOL, LSE_TOL, GRAD_REL, GRAD_FLOOR = 1e-2, 2e-3, 2e-2, 1e-3
-
-
-def f64(t):
-    return t.detach().to("cpu", torch.float64).numpy()
-
-
-def run_gpu(fa, q, k, v, do, causal, scale, backward=True):
-    dev = torch.device("cuda", 0)
-    qd, kd, vd = (x.to(dev) for x in (q, k, v))
-    out, lse = fa.attention_forward(qd, kd, vd, causal, scale)
-    res = {"out": out, "lse": lse}
-    if backward:
-        dod = do.to(dev)
-        res["dq"], res["dk"], res["dv"] = fa.attention_backward(qd, kd, vd, out, dod, lse,
-                                                                causal, scale)
-    torch.cuda.synchronize()
-    assert fa.fa_last_device_status() == 0
-    return {name: f64(t) for name, t in res.items()}
-
-
-def check_fwd(got, out_ref, lse_ref):
-    e_out = np.abs(got["out"] - out_ref).max()
-    e_lse = np.abs(got["lse"] - lse_ref).max()
-    assert np.isfinite(got["out"]).all() and np.isfinite(got["lse"]).all()
-    assert e_out <= OUT_TOL, f"out max-abs {e_out:.3e}"
-    assert e_lse <= LSE_TOL, f"lse max-abs {e_lse:.3e}"
-
-
-def check_grad(name, got, ref):
-    assert np.isfinite(got).all(), name
-    bound = GRAD_REL * max(np.abs(ref).max(), GRAD_FLOOR)
-    err = np.abs(got - ref).max()
-    assert err <= bound, f"{name} max-abs {err:.3e} > {bound:.3e}"
-
-
-@pytest.fixture(scope="module")
-def fa(fa_lib):
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    return fa_lib
+from parity import (GRAD_FLOOR, GRAD_REL, LSE_TOL, OUT_TOL, check_fwd, check_grad, f64,
+                    run_gpu)
 
 
 # ------------------------------------------------------------ full size --
