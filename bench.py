@@ -401,8 +401,9 @@ def main():
     step_flops = flops(w, True, w.backward)
     e = elem_bytes(w)
     in_bytes = 2 * tensor_bytes(w.B, w.Hq, w.S, w.d, e) + 2 * tensor_bytes(w.B, w.Hkv, w.kv_len, w.d, e)
-    l2_note = (f"inputs larger than L2: Q,K,V,dO = {in_bytes / 2**20:.0f} MiB "
-               f"read per step vs {L2_BYTES / 2**20:.0f} MiB L2; no flush")
+    l2_note = (f"inputs {'larger' if in_bytes > L2_BYTES else 'NOT larger'} than L2: "
+               f"Q,K,V,dO = {in_bytes / 2**20:.0f} MiB read per step vs "
+               f"{L2_BYTES / 2**20:.0f} MiB L2; no flush")
     config = {"workload": w.describe(), "global_batch": w.B * world, "seq_len": w.S,
               "heads": [w.Hq, w.Hkv], "head_dim": w.d, "causal": w.causal,
               "parallelism": f"replicas x{world}", "l2": l2_note}
