@@ -28,9 +28,10 @@
 //
 // Warp roles of bwd_main (320 threads): warp 0 TMA producer (K_j, V_j once;
 // Q_i, dO_i, L_i, D_i through a 2-stage ring), warp 1 MMA issuer and TMEM
-// owner, warps 2-5 compute P^T and dS^T (one thread per key row), warps 6-9
-// move dQ from TMEM to the global accumulator (one thread per query row);
-// at the end warps 2-5 write dK and warps 6-9 write dV.
+// owner, warps 2-9 compute P^T and dS^T (one thread per key row, two warps per
+// TMEM lane quarter splitting the step's 128 query columns) and then move
+// their half of dQ from TMEM into the global accumulator; at the end warps
+// 2-5 write dK and warps 6-9 write dV.
 //
 // Tensor memory: dK [0,d), dV [128,128+d), S^T / P^T [256,384),
 // dP^T / dQ [384,512). dQ reuses dP^T's columns once the softmax warps have
@@ -195,15 +196,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(qdo_full(s), 1);
-      mbar_init(qdo_empty(s), 1 + 4);   // MMA commit + one per softmax warp
+      mbar_init(qdo_empty(s), 1 + 8);   // MMA commit + one per compute warp
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 4);
-    mbar_init(ds_full, 4);
+    mbar_init(p_full, 8);
+    mbar_init(ds_full, 8);
     mbar_init(dv_done, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 4);
+    mbar_init(dq_empty, 8);
     mbar_init(ds_empty, 1);
     mbar_init(kd_done, 1);
     mbar_init(drain, 1);
@@ -262,10 +263,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ===================== MMA issuer =====================
-    // Issue order per step n (S^T(n+1) goes ahead of dQ(n) so the softmax warps
-    // compute P(n+1) while the tensor core finishes step n):
-    //   dV(n) [P(n) ready]  dK(n) [dS(n) ready]  S^T(n+1) [dV(n) done: P(n) read]
-    //   dQ(n)  dP^T(n+1) [dQ(n) read out of TMEM]
+    // Issue order per step n (dQ(n) first, so that its read-out and dP^T(n+1)
+    // follow soon after dS(n); S^T(n+1) as soon as dV(n) has read P^T(n)):
+    //   dV(n) [P(n) ready]  dQ(n) [dS(n) ready]  S^T(n+1) [dV(n) done]
+    //   dK(n)  dP^T(n+1) [dQ(n) read out of TMEM]
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kTileM, kBf16, false, false);  // S^T, dP^T
       constexpr uint32_t idesc_kv = make_idesc(128, D, kBf16, false, true);       // dV, dK
@@ -309,35 +310,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = n % NS;
         const int st1 = (n + 1) % NS;
         const bool more = n + 1 < n_iter;
-        // dV += P^T dO_i  (P^T from TMEM, 16-bit packed in S^T's first 64 columns)
+        // dV += P^T dO_i  (P^T from TMEM, 16-bit packed: query columns 0-63 in
+        // S^T's columns 0-31, columns 64-127 in S^T's columns 96-127)
         if (!(ok = mbar_wait(p_full, n & 1, abort_flag, p.status))) break;
         tr(1);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTileM / 16; ++ks)
-          mma_ts(t_dv, t_s + ks * 8, make_sdesc(do_s(st) + ks * 2048, kTileM * 128, 1024),
-                 idesc_kv, (n > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(t_dv, t_s + ks * 8 + (ks >= 4 ? 64 : 0),
+                 make_sdesc(do_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
+                 (n > 0 || ks > 0) ? 1u : 0u);
         tc_commit(dv_done);
-        // dK += dS^T Q_i
+        // dQ (into dP^T's columns: the compute warps have read dP^T(n))
         if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, p.status))) break;
         tr(3);
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kTileM / 16; ++ks)
-          mma_ss(t_dk, make_sdesc(ds_s + (ks / 4) * (kTileN * 128) + (ks % 4) * 32, 16, 1024),
-                 make_sdesc(q_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
-                 (n > 0 || ks > 0) ? 1u : 0u);
-        // S^T for the next step, once dV(n) has consumed P^T(n)
-        if (more) {
-          if (!(ok = mbar_wait(qdo_full(st1), static_cast<uint32_t>((n + 1) / NS) & 1,
-                               abort_flag, p.status)))
-            break;
-          if (!(ok = mbar_wait(dv_done, n & 1, abort_flag, p.status))) break;
-          tr(5);
-          tc_fence_after();
-          issue_s(st1);
-        }
-        // dQ (into dP^T's columns: the softmax warps have read dP^T(n))
 #pragma unroll
         for (int ks = 0; ks < kTileN / 16; ++ks) {
           if constexpr (kDqT)   // dQ^T = K_j^T dS^T
@@ -348,6 +335,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
         }
         tc_commit(dq_full);
+        // S^T for the next step, once dV(n) has consumed P^T(n)
+        if (more) {
+          if (!(ok = mbar_wait(qdo_full(st1), static_cast<uint32_t>((n + 1) / NS) & 1,
+                               abort_flag, p.status)))
+            break;
+          if (!(ok = mbar_wait(dv_done, n & 1, abort_flag, p.status))) break;
+          tr(5);
+          tc_fence_after();
+          issue_s(st1);
+        }
+        // dK += dS^T Q_i; then dS^T and stage st (Q_i, dO_i) are free
+#pragma unroll
+        for (int ks = 0; ks < kTileM / 16; ++ks)
+          mma_ss(t_dk, make_sdesc(ds_s + (ks / 4) * (kTileN * 128) + (ks % 4) * 32, 16, 1024),
+                 make_sdesc(q_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
+                 (n > 0 || ks > 0) ? 1u : 0u);
         tc_commit(ds_empty);
         tc_commit(qdo_empty(st));
         tr(6);
@@ -362,16 +365,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_commit(ok ? kd_done : drain);
       if (!ok) drain_wait(drain, 0, p.status);
     }
-  } else if (warp < 6) {
-    // ===================== P^T and dS^T (one thread per key row) =====================
+  } else {
+    // ============ P^T, dS^T and the dQ read-out (warps 2-9) ============
+    // Two warps per TMEM lane quarter, one thread per key row: warps 2-5 take
+    // query columns 0-63 of the step (half 0), warps 6-9 columns 64-127
+    // (half 1). Each warp writes its packed P^T over score columns it has
+    // read itself (half 0: columns 0-31, half 1: 96-127), so the two warps of
+    // a quarter never wait for each other.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int c0 = half * 64;                   // first query column of this warp
     const int r = quarter * 32 + lane;
     const int kv = j * kTileN + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + 256;
     const uint32_t t_dp = tmem + lane_off + 384;
     const float c = p.scale_log2;
-    uint8_t* ds_row = smem + Cfg::kOffDS + r * 128;
+    // dS^T row r of 64-column chunk `half` of the 128-byte-swizzled tile
+    uint8_t* ds_row = smem + Cfg::kOffDS + half * (kTileN * 128) + r * 128;
     Tracer tr((warp == 2 && lane == 0) ? p.trace : nullptr, 2);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
@@ -379,40 +390,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t par = static_cast<uint32_t>(it / NS) & 1;
       const int i = i_of(it);
       const float* rowv = reinterpret_cast<const float*>(smem + Cfg::kOffRow + st * 1024);
-      const float* l2s = rowv;          // L * log2(e) per query column
-      const float* dls = rowv + 128;    // D per query column
+      const float* l2s = rowv + c0;          // L * log2(e) per query column
+      const float* dls = rowv + 128 + c0;    // D per query column
       ok = __all_sync(0xffffffffu, mbar_wait(qdo_full(st), par, abort_flag, p.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, p.status));
       if (!ok) break;
       tr(20);
       tc_fence_after();
       // Masked entries: key past the sequence end, or (causal) key after the
-      // query's position q + kv_offset. Column qc of this row is masked iff
-      // qc < thr; thr <= 0 on every tile that is neither diagonal nor ragged,
-      // which skip the selects.
-      const int q0 = i * kTileM;
-      const int thr = kv >= p.Skv ? kTileM : (p.causal ? min(kv - p.kv_offset - q0, kTileM) : 0);
+      // query's position q + kv_offset. Column e of this warp's half is masked
+      // iff e < thr; thr <= 0 on every tile that is neither diagonal nor
+      // ragged, which skip the selects.
+      const int q0 = i * kTileM + c0;
+      const int thr = kv >= p.Skv ? 64 : (p.causal ? min(kv - p.kv_offset - q0, 64) : 0);
       const bool any_mask = __any_sync(0xffffffffu, thr > 0);
-      uint32_t ppk[64];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      uint32_t ppk[32];
+      {
         uint32_t raw[64];
-        tmem_ld32(t_s + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
-        tmem_ld32(t_s + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+        tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
+        tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
         tmem_wait_ld();
         if (any_mask) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            raw[e] = (h * 64 + e < thr) ? __float_as_uint(-INFINITY) : raw[e];
+          for (int e = 0; e < 64; ++e) raw[e] = (e < thr) ? __float_as_uint(-INFINITY) : raw[e];
         }
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const int qc = h * 64 + e;
-          const float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[qc]));
-          const float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[qc + 1]));
-          ppk[h * 32 + e / 2] = pack2<kBf16>(p0, p1);
+          const float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[e]));
+          const float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[e + 1]));
+          ppk[e / 2] = pack2<kBf16>(p0, p1);
         }
-        tmem_st32(t_s + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(ppk + h * 32));
+        tmem_st32(t_s + half * 96, ppk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -425,27 +433,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tr(22);
       tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      {
         uint32_t raw[64];
-        tmem_ld32(t_dp + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
-        tmem_ld32(t_dp + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+        tmem_ld32(t_dp + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
+        tmem_ld32(t_dp + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
         tmem_wait_ld();
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const int qc = h * 64 + e;
-          const float2 pp = unpack2<kBf16>(ppk[h * 32 + e / 2]);
-          const float d0 = pp.x * (__uint_as_float(raw[e]) - dls[qc]);
-          const float d1 = pp.y * (__uint_as_float(raw[e + 1]) - dls[qc + 1]);
+          const float2 pp = unpack2<kBf16>(ppk[e / 2]);
+          const float d0 = pp.x * (__uint_as_float(raw[e]) - dls[e]);
+          const float d1 = pp.y * (__uint_as_float(raw[e + 1]) - dls[e + 1]);
           w[e / 2] = pack2<kBf16>(d0, d1);
         }
-        // 64 query columns = one 128-byte row of chunk h; 16-byte unit u of
-        // row r sits at unit u ^ (r % 8) (128-byte swizzle)
-        uint8_t* chunk_row = ds_row + h * (kTileN * 128);
+        // this warp's 64 query columns = one 128-byte row of chunk `half`;
+        // 16-byte unit u of row r sits at unit u ^ (r % 8) (128-byte swizzle)
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(chunk_row + ((u ^ (r & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
               make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       }
       fence_proxy_async_smem();
@@ -456,91 +461,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(qdo_empty(st));
       }
       tr(23);
+
+      // dQ(it): TMEM -> fp32 accumulator. d = 128: dQ^T (TMEM lanes = head
+      // dimension), the warp holds head-dimension entries of its quarter for
+      // its 64 query rows;
+      // d = 64: dQ (TMEM lanes = query rows), this thread adds 32 head-dimension
+      // entries (half `half`) of its query row with 16-byte reductions.
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
+      if (!ok) break;
+      tr(30);
+      tc_fence_after();
+      constexpr int kCols = kDqT ? 64 : 32;
+      uint32_t acc[kCols];
+#pragma unroll
+      for (int cc = 0; cc < kCols / 32; ++cc)
+        tmem_ld32(t_dp + (kDqT ? c0 : half * 32) + cc * 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+      tr(31);
+      const int bh = bh_of(it);
+      float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM) * D;
+      if constexpr (kDqT) {
+        float* col = tile + static_cast<size_t>(c0) * D + r;
+#pragma unroll
+        for (int q = 0; q < 64; ++q) atomicAdd(col + q * D, __uint_as_float(acc[q]));
+      } else {
+        float4* row = reinterpret_cast<float4*>(tile + static_cast<size_t>(r) * D + half * 32);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          atomicAdd(row + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                         __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
+      }
+      tr(32);
     }
-    // ---- epilogue: dK = scale * accumulated dS^T Q ----
+    // ---- epilogue: warps 2-5 write dK = scale * accumulated dS^T Q, warps 6-9 dV ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
     if (ok) {
       tc_fence_after();
       using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      Elem* dst = reinterpret_cast<Elem*>(p.dk) + (static_cast<size_t>(bkv) * p.Skv + kv) * D;
+      const float f = half == 0 ? p.scale : 1.f;
+      Elem* dst = reinterpret_cast<Elem*>(half == 0 ? p.dk : p.dv) +
+                  (static_cast<size_t>(bkv) * p.Skv + kv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + cc * 32, o);
+        tmem_ld32(tmem + lane_off + half * 128 + cc * 32, o);
         tmem_wait_ld();
         if (kv < p.Skv) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             d4[v] = make_uint4(
-                pack2<kBf16>(__uint_as_float(o[8 * v]) * p.scale, __uint_as_float(o[8 * v + 1]) * p.scale),
-                pack2<kBf16>(__uint_as_float(o[8 * v + 2]) * p.scale, __uint_as_float(o[8 * v + 3]) * p.scale),
-                pack2<kBf16>(__uint_as_float(o[8 * v + 4]) * p.scale, __uint_as_float(o[8 * v + 5]) * p.scale),
-                pack2<kBf16>(__uint_as_float(o[8 * v + 6]) * p.scale, __uint_as_float(o[8 * v + 7]) * p.scale));
-        }
-      }
-    }
-  } else {
-    // ===================== dQ: TMEM -> fp32 accumulator =====================
-    // d = 128: thread = head-dimension index, reading its dQ^T row (128 query
-    // columns); d = 64: thread = query row, reading its d values.
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_dq = tmem + lane_off + 384;
-    constexpr int kCols = kDqT ? kTileM : D;
-    Tracer tr((warp == 6 && lane == 0) ? p.trace : nullptr, 3);
-    bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
-      if (!ok) break;
-      tr(30);
-      tc_fence_after();
-      uint32_t acc[kCols];
-#pragma unroll
-      for (int cc = 0; cc < kCols / 32; ++cc)
-        tmem_ld32(t_dq + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
-      tr(31);
-      const int bh = bh_of(it), i = i_of(it);
-      float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM) * D;
-      if constexpr (kDqT) {
-        // warp-wide: 32 consecutive head-dimension entries of one query row
-        float* col = tile + r;
-#pragma unroll
-        for (int q = 0; q < kTileM; ++q) atomicAdd(col + q * D, __uint_as_float(acc[q]));
-      } else {
-        float4* row = reinterpret_cast<float4*>(tile + static_cast<size_t>(r) * D);
-#pragma unroll
-        for (int v = 0; v < D / 4; ++v)
-          atomicAdd(row + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
-                                         __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
-      }
-      tr(32);
-    }
-    // ---- epilogue: dV ----
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
-    if (ok) {
-      tc_fence_after();
-      const int kv = j * kTileN + r;
-      using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      Elem* dst = reinterpret_cast<Elem*>(p.dv) + (static_cast<size_t>(bkv) * p.Skv + kv) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + 128 + cc * 32, o);
-        tmem_wait_ld();
-        if (kv < p.Skv) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            d4[v] = make_uint4(pack2<kBf16>(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
-                               pack2<kBf16>(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
-                               pack2<kBf16>(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
-                               pack2<kBf16>(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+                pack2<kBf16>(__uint_as_float(o[8 * v]) * f, __uint_as_float(o[8 * v + 1]) * f),
+                pack2<kBf16>(__uint_as_float(o[8 * v + 2]) * f, __uint_as_float(o[8 * v + 3]) * f),
+                pack2<kBf16>(__uint_as_float(o[8 * v + 4]) * f, __uint_as_float(o[8 * v + 5]) * f),
+                pack2<kBf16>(__uint_as_float(o[8 * v + 6]) * f, __uint_as_float(o[8 * v + 7]) * f));
         }
       }
     }
