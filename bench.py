@@ -252,9 +252,19 @@ def run_gpu(args, w, rank, world, local_rank):
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     ws = fa.workspace_for(qd, kd)
     stream = torch.cuda.current_stream(dev)
-    # self-attention through fa_fwd / fa_bwd; separate lengths through the *_kv calls
+    # self-attention through fa_fwd / fa_bwd; separate lengths through the *_kv
+    # calls; decode workloads (few query rows) through the split-KV forward
     fwd_call = fa.fa_fwd if w.S == w.kv_len else fa.fa_fwd_kv
     bwd_call = fa.fa_bwd if w.S == w.kv_len else fa.fa_bwd_kv
+    dec_ws_bytes = 0
+    if w.decode:
+        dec_ws_bytes = fa.fa_fwd_splitkv_workspace_bytes(w.B, w.Hq, w.Hkv, w.S, w.kv_len, w.d, 0)
+        dec_ws = [torch.empty(max(dec_ws_bytes, 1), dtype=torch.uint8, device=dev) for _ in range(2)]
+
+        def fwd_call(q_, k_, v_, o_, l_, causal, scale, st, _ws=dec_ws):
+            ws_ = _ws[1] if (q_.data_ptr() != qd.data_ptr()) else _ws[0]
+            fa.fa_fwd_splitkv(q_, k_, v_, o_, l_, causal, scale, 0,
+                              ws_ if dec_ws_bytes else None, st)
 
     def step():
         fwd_call(qd, kd, vd, out, lse, w.causal, w.scale, stream)
@@ -368,7 +378,8 @@ def run_gpu(args, w, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms, fwd_ms, bwd_ms, e2e_ms = t.tolist()
     return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms,
-                h2d=h2d, d2h=d2h, clocks=clocks.summary(), dist=dist)
+                h2d=h2d, d2h=d2h, clocks=clocks.summary(), dist=dist,
+                launches_per_fwd=(2 if dec_ws_bytes else 1))
 
 
 def main():
@@ -491,11 +502,22 @@ def main():
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
                 "pipelining": "2 device buffer sets; H2D of step k and D2H of step k-1 on copy "
                               "streams overlap step k's kernels"},
-        "gpu_launches": (4 if w.backward else 1) * K,
+        "gpu_launches": (r["launches_per_fwd"] + (3 if w.backward else 0)) * K,
         "clocks": r["clocks"],
     }
     if not w.backward:   # forward-only workload: the forward kernel is the whole step
         line["roofline"] = dict(line["roofline_fwd"])
+    if w.decode:
+        # few query rows: the split-KV forward streams K and V once; HBM-bound
+        gbs = fwd_algorithmic_bytes(w) / (r["fwd_ms"] * 1e-3) / 1e9
+        line["roofline"] = {
+            "kernel": "fa_decode_kernel + decode_merge_kernel (timed as the fa_fwd_splitkv call)",
+            "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+            "algorithmic_bytes": fwd_algorithmic_bytes(w),
+            "peak_source": f"{peak_src} hbm_gbs (copy)",
+        }
+        line["roofline_fwd"] = dict(line["roofline"])
     if world == 1 and not args.no_cpu_baseline:
         cores, how = cpu_threads()
         total_t, total_f = 0.0, 0

@@ -2,7 +2,8 @@
 libfa (include/fa.h).
 
 The functions with the C names (`fa_fwd`, `fa_bwd`, `fa_bwd_workspace_bytes`,
-`fa_fwd_kv`, `fa_bwd_kv`, `fa_bwd_kv_workspace_bytes`, `fa_strerror`,
+`fa_fwd_kv`, `fa_bwd_kv`, `fa_bwd_kv_workspace_bytes`, `fa_fwd_splitkv`,
+`fa_fwd_splitkv_workspace_bytes`, `fa_strerror`,
 `fa_last_device_status`, `fa_version`) only marshal arguments:
 shapes come from the tensors, pointers from `data_ptr()`, and the stream from
 PyTorch's current stream. Every step of the computation runs in libfa's CUDA
@@ -25,7 +26,8 @@ __all__ = [
     "FAError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_strerror",
     "fa_last_device_status", "fa_version", "attention_forward", "attention_backward",
     "DTYPE_CODES", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_fwd_kv", "fa_bwd_kv",
-    "fa_bwd_kv_workspace_bytes",
+    "fa_bwd_kv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes",
+    "decode_forward",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
@@ -61,6 +63,10 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_kv_workspace_bytes.restype = sz
     L.fa_bwd_kv.argtypes = [vp] * 9 + [i32] * 7 + [f32, i32, vp, sz, vp]
     L.fa_bwd_kv.restype = i32
+    L.fa_fwd_splitkv.argtypes = [vp] * 5 + [i32] * 7 + [f32, i32, i32, vp, sz, vp]
+    L.fa_fwd_splitkv.restype = i32
+    L.fa_fwd_splitkv_workspace_bytes.argtypes = [i32] * 7
+    L.fa_fwd_splitkv_workspace_bytes.restype = sz
     L.fa_strerror.argtypes = [i32]
     L.fa_strerror.restype = ctypes.c_char_p
     L.fa_last_device_status.argtypes = [vp, ctypes.POINTER(i32)]
@@ -174,6 +180,38 @@ def fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale
                          _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_bwd_kv")
+
+
+def fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d, n_splits=0) -> int:
+    return int(lib().fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d, n_splits))
+
+
+def fa_fwd_splitkv(q, k, v, out, lse, causal=True, scale=None, n_splits=0, workspace=None,
+                   stream=None):
+    """Call fa_fwd_splitkv (few query rows against a long key/value sequence);
+    `workspace` is a device tensor of at least fa_fwd_splitkv_workspace_bytes(...)
+    bytes, or None when that size is 0."""
+    _check_contig(q, k, v, out, lse)
+    B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
+                              Skv, d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
+                              int(n_splits), _ptr(workspace), ws_bytes, _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_fwd_splitkv")
+
+
+def decode_forward(q, k, v, causal=True, scale=None, n_splits=0, stream=None):
+    """Allocate out, lse and the split workspace with PyTorch and run
+    fa_fwd_splitkv. Returns (out, lse)."""
+    B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    n = fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d, n_splits)
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    fa_fwd_splitkv(q, k, v, out, lse, causal, scale, n_splits, ws, stream)
+    return out, lse
 
 
 def fa_last_device_status(stream=None) -> int:

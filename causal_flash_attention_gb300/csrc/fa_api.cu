@@ -1,11 +1,13 @@
 // C-ABI entry points of libfa (declared in include/fa.h): argument checks,
 // TMA descriptor construction and kernel launches. No device memory is
 // allocated here; the only device-resident state is the status word below.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 
 #include "../../include/fa.h"
+#include "fa_decode.h"
 #include "fa_internal.h"
 
 namespace fa {
@@ -96,6 +98,37 @@ WsLayout ws_layout(int B, int Hq, int Sq, int d) {
   w.lse2 = w.delta + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
   w.total = w.lse2 + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
   return w;
+}
+
+// Split-KV plan of fa_fwd_splitkv: key tiles per CTA, CTA count per (batch,
+// key/value head) and the partial-result workspace. Automatic choice: enough
+// ranges for two CTAs per SM of the 152-SM part, never an empty range.
+constexpr int kDecodeTargetCtas = 2 * 152;
+constexpr int kDecodeMaxRows = 128;   // G * Sq rows must fit one query tile
+
+struct SplitPlan {
+  int n_splits, tiles_per_split, R;
+  size_t part_out, part_lse2, total;
+};
+
+SplitPlan split_plan(int B, int Hq, int Hkv, int Sq, int Skv, int d, int n_splits_req) {
+  SplitPlan sp;
+  const int n_tiles = (Skv + kTileN - 1) / kTileN;
+  const long long bhkv = static_cast<long long>(B) * Hkv;
+  long long want = n_splits_req > 0 ? n_splits_req : (kDecodeTargetCtas + bhkv - 1) / bhkv;
+  want = std::max(1LL, std::min<long long>(want, n_tiles));
+  sp.tiles_per_split = static_cast<int>((n_tiles + want - 1) / want);
+  sp.n_splits = (n_tiles + sp.tiles_per_split - 1) / sp.tiles_per_split;
+  sp.R = (Hq / Hkv) * Sq;
+  sp.part_out = 0;
+  if (sp.n_splits == 1) {
+    sp.part_lse2 = sp.total = 0;
+  } else {
+    const long long rows = bhkv * sp.n_splits * sp.R;
+    sp.part_lse2 = static_cast<size_t>(round_up(rows * d * 4, 256));
+    sp.total = sp.part_lse2 + static_cast<size_t>(round_up(rows * 4, 256));
+  }
+  return sp;
 }
 
 }  // namespace
@@ -278,6 +311,67 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* out, const v
            fa_stream_t stream) {
   return fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, S, S, d, causal, scale, dtype,
                    workspace, workspace_bytes, stream);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                      int n_splits) {
+  if (check_common(B, Hq, Hkv, Sq, Skv, d, 0, 1.f, FA_BF16) != FA_OK || n_splits < 0 ||
+      (Hq / Hkv) * Sq > kDecodeMaxRows)
+    return 0;
+  return split_plan(B, Hq, Hkv, Sq, Skv, d, n_splits).total;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Skv, int d, int causal, float scale, int dtype,
+                   int n_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (n_splits < 0 || (Hq / Hkv) * Sq > kDecodeMaxRows) return FA_ERR_SHAPE;
+  if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if (dtype == FA_F32)   // plain fp32 arithmetic: one warp per query row, no split
+    return fa_fwd_kv(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype, stream);
+
+  const SplitPlan sp = split_plan(B, Hq, Hkv, Sq, Skv, d, n_splits);
+  if (sp.total > 0 && (!workspace || workspace_bytes < sp.total)) return FA_ERR_WORKSPACE;
+  if (sp.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == FA_BF16;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16))
+    return FA_ERR_TMA;
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.part_out = sp.total ? reinterpret_cast<float*>(wsb + sp.part_out) : nullptr;
+  p.part_lse2 = sp.total ? reinterpret_cast<float*>(wsb + sp.part_lse2) : nullptr;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv;
+  p.kv_offset = causal ? Skv - Sq : 0;
+  p.causal = causal != 0;
+  p.G = Hq / Hkv;
+  p.R = sp.R;
+  p.n_kv_tiles = (Skv + kTileN - 1) / kTileN;
+  p.tiles_per_split = sp.tiles_per_split;
+  p.n_splits = sp.n_splits;
+  p.scale_log2 = scale * kLog2e;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  if (launch_decode(p, d, bf16, st) != cudaSuccess) return FA_ERR_CUDA;
+  if (sp.n_splits == 1) return FA_OK;
+
+  DecodeMergeParams m;
+  m.part_out = p.part_out;
+  m.part_lse2 = p.part_lse2;
+  m.out = out;
+  m.lse = lse;
+  m.B = B; m.Hq = Hq; m.Hkv = Hkv; m.Sq = Sq; m.G = p.G; m.R = p.R; m.d = d;
+  m.n_splits = sp.n_splits;
+  m.dtype = dtype;
+  return launch_decode_merge(m, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_last_device_status(fa_stream_t stream, int* status) {

@@ -19,6 +19,10 @@ Workloads (shapes in [B, H, S, d] order, Q/dO with Hq heads, K/V with Hkv):
   prefill_8k   bf16,  B=1 Hq=32 Hkv=8 Sq=2048 Skv=8192 d=128, N(0,1), seed 5:
                a 2048-query chunk at the end of an 8192-position context
                (causal mask aligned to the last key, kv_offset = Skv - Sq)
+  decode_8k    bf16,  B=16 Hq=32 Hkv=8 Sq=1 Skv=8192 d=128, N(0,1), seed 6,
+               forward only: one new token per sequence over an 8192-key cache
+  spec_32k     bf16,  B=2 Hq=32 Hkv=8 Sq=4 Skv=32768 d=128, N(0,1), seed 7,
+               forward only: four new tokens over a 32768-key cache
 
 All use scale = 1/sqrt(d); all but the *_nc workloads use causal masking.
 S is the query length; K and V have `kv_len` rows (S unless Skv is given).
@@ -49,6 +53,7 @@ class Workload:
     spike_every: int = 0          # if > 0: K rows at positions % spike_every == 0 ...
     spike_scale: float = 1.0      # ... are multiplied by this before rounding
     Skv: int = 0                  # key/value length; 0 means the same as S
+    decode: bool = False          # few query rows: timed through the split-KV forward
 
     @property
     def kv_len(self) -> int:
@@ -86,6 +91,10 @@ WORKLOADS = {
         Workload("long_8k_nc", "bf16", 1, 32, 32, 8192, 128, seed=3, causal=False,
                  value_scale=0.5, spike_every=512, spike_scale=8.0),
         Workload("prefill_8k", "bf16", 1, 32, 8, 2048, 128, seed=5, Skv=8192),
+        Workload("decode_8k", "bf16", 16, 32, 8, 1, 128, seed=6, Skv=8192, backward=False,
+                 decode=True),
+        Workload("spec_32k", "bf16", 2, 32, 8, 4, 128, seed=7, Skv=32768, backward=False,
+                 decode=True),
     ]
 }
 

@@ -136,6 +136,38 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out,
               fa_stream_t stream);
 
 /*
+ * Split-KV forward for few query rows per head: decode (one or a few new
+ * tokens, Sq small, against a long key/value cache Skv). Same arguments,
+ * layouts, mask (kv_offset = Skv - Sq under causal) and results as fa_fwd_kv;
+ * only the work layout differs. The G = Hq / Hkv query heads of a key/value
+ * head are packed into one 128-row tile, so G * Sq must be at most 128
+ * (else FA_ERR_SHAPE); the key/value sequence of each (batch, key/value head)
+ * is cut into n_splits ranges of whole 128-key tiles processed in parallel,
+ * each producing a partial out and log-sum-exp, which a second kernel merges
+ * ("Phase 14: Flash Attention 2 for SM120", section 已知局限与后续优化方向,
+ * item 1: a dedicated decode kernel that reduces in parallel along the
+ * key/value dimension).
+ *
+ * n_splits: 0 = automatic (about two CTAs per SM); otherwise the requested
+ * number of ranges, reduced so that no range is empty (at most ceil(Skv/128)).
+ * workspace: caller-owned device memory of at least
+ * fa_fwd_splitkv_workspace_bytes(...) bytes, 256-byte aligned, for the
+ * per-range partial results (fp32); it may be NULL when that size is 0 (one
+ * range). FA_F32 inputs take the fa_fwd_kv path (no split, no workspace).
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse,
+                   int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                   float scale, int dtype, int n_splits, void* workspace,
+                   size_t workspace_bytes, fa_stream_t stream);
+
+/* Workspace bytes of fa_fwd_splitkv for these sizes and n_splits (0 =
+ * automatic): B * Hkv * ranges * G * Sq rows of d + 1 floats, each region
+ * 256-byte aligned; 0 when one range suffices, and 0 for invalid sizes (the
+ * call reports those). */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                      int n_splits);
+
+/*
  * Size of the fixed device scratch array behind fa_bwd_noalloc (32 MiB). A
  * call fits when fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) is at most this,
  * e.g. B*Hq = 96 heads at S = 1024, d = 64 (about 25.9 MB).

@@ -157,3 +157,44 @@ def test_kv_workspace_is_sized_by_the_query_length(fa_lib):
     assert fa_lib.fa_bwd_kv_workspace_bytes(1, 2, 2, 128, 0, 64) == 0
     assert fa_lib.fa_bwd_kv_workspace_bytes(1, 2, 2, 128, 128, 64) == \
         fa_lib.fa_bwd_workspace_bytes(1, 2, 2, 128, 64)
+
+
+# split-KV forward (fa_fwd_splitkv)
+def _splitkv(L, q=16, k=16, v=16, out=16, lse=16, B=1, Hq=8, Hkv=2, Sq=1, Skv=4096, d=128,
+             causal=1, scale=0.125, dtype=2, n_splits=0, ws=256, ws_bytes=1 << 30):
+    return L.fa_fwd_splitkv(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype,
+                            n_splits, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Sq=33, Hq=16, Hkv=4), FA_ERR_SHAPE),           # G * Sq = 132 > 128 rows
+    (dict(Sq=32, Hq=16, Hkv=4, q=None), FA_ERR_NULL),     # G * Sq = 128 fits
+    (dict(n_splits=-1), FA_ERR_SHAPE), (dict(Sq=5000), FA_ERR_SHAPE),
+    (dict(Skv=0), FA_ERR_SHAPE), (dict(d=96), FA_ERR_SHAPE), (dict(dtype=4), FA_ERR_DTYPE),
+    (dict(scale=-2.0), FA_ERR_SCALE), (dict(lse=None), FA_ERR_NULL), (dict(v=40), FA_ERR_ALIGN),
+])
+def test_splitkv_rejects_bad_arguments(fa_lib, kw, code):
+    assert _splitkv(fa_lib.lib(), **kw) == code
+
+
+def test_splitkv_workspace_plan(fa_lib):
+    up = lambda x, m: (x + m - 1) // m * m
+    ws = fa_lib.fa_fwd_splitkv_workspace_bytes
+
+    def expect(B, Hq, Hkv, Sq, Skv, d, n_req):
+        tiles = (Skv + 127) // 128
+        want = n_req if n_req > 0 else -(-2 * 152 // (B * Hkv))
+        want = max(1, min(want, tiles))
+        per = -(-tiles // want)
+        n = -(-tiles // per)
+        if n == 1:
+            return 0
+        rows = B * Hkv * n * (Hq // Hkv) * Sq
+        return up(rows * d * 4, 256) + up(rows * 4, 256)
+
+    for args in [(16, 32, 8, 1, 8192, 128, 0), (1, 8, 2, 4, 4096, 64, 0), (2, 4, 4, 1, 100, 128, 0),
+                 (1, 8, 1, 16, 65536, 128, 7), (1, 2, 2, 1, 300, 64, 1), (64, 32, 8, 1, 1024, 128, 0)]:
+        assert ws(*args) == expect(*args), args
+    assert ws(1, 8, 2, 1, 4096, 128, 0) > 0
+    assert ws(1, 2, 2, 1, 128, 128, 0) == 0          # one key tile: one range, no workspace
+    assert ws(1, 16, 4, 33, 4096, 128, 0) == 0       # invalid: G * Sq > 128
