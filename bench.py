@@ -96,7 +96,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"),
-                  "fa_bwd_kernel": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h")}
+                  "fa_bwd_kernel": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
+                  "fa_decode_kernel": ("fa_decode.cu", "ptx.cuh", "fa_internal.h", "fa_decode.h")}
 
 
 def kernel_source_hash(kernel):
@@ -513,7 +514,9 @@ def main():
         line["roofline"] = {
             "kernel": "fa_decode_kernel + decode_merge_kernel (timed as the fa_fwd_splitkv call)",
             "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+            "frac": gbs / peaks["hbm_gbs"],
+            "traffic": None if args.heads else recorded_traffic("fa_decode_kernel", w.name),
+            "traffic_unit": "bytes per launch (dram read + write)",
             "algorithmic_bytes": fwd_algorithmic_bytes(w),
             "peak_source": f"{peak_src} hbm_gbs (copy)",
         }

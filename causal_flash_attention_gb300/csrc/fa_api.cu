@@ -101,9 +101,12 @@ WsLayout ws_layout(int B, int Hq, int Sq, int d) {
 }
 
 // Split-KV plan of fa_fwd_splitkv: key tiles per CTA, CTA count per (batch,
-// key/value head) and the partial-result workspace. Automatic choice: enough
-// ranges for two CTAs per SM of the 152-SM part, never an empty range.
-constexpr int kDecodeTargetCtas = 2 * 152;
+// key/value head) and the partial-result workspace. One CTA fits on an SM at a
+// time and each CTA pays a start-up (barriers, tensor memory, query staging,
+// first-load latency), so the automatic choice is the largest range count that
+// keeps every CTA in one wave on the 152 SMs (one range when the (batch,
+// key/value head) pairs alone fill the GPU), never an empty range.
+constexpr int kDecodeWaveCtas = 152;
 constexpr int kDecodeMaxRows = 128;   // G * Sq rows must fit one query tile
 
 struct SplitPlan {
@@ -115,7 +118,7 @@ SplitPlan split_plan(int B, int Hq, int Hkv, int Sq, int Skv, int d, int n_split
   SplitPlan sp;
   const int n_tiles = (Skv + kTileN - 1) / kTileN;
   const long long bhkv = static_cast<long long>(B) * Hkv;
-  long long want = n_splits_req > 0 ? n_splits_req : (kDecodeTargetCtas + bhkv - 1) / bhkv;
+  long long want = n_splits_req > 0 ? n_splits_req : kDecodeWaveCtas / bhkv;
   want = std::max(1LL, std::min<long long>(want, n_tiles));
   sp.tiles_per_split = static_cast<int>((n_tiles + want - 1) / want);
   sp.n_splits = (n_tiles + sp.tiles_per_split - 1) / sp.tiles_per_split;

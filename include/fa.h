@@ -148,7 +148,8 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out,
  * item 1: a dedicated decode kernel that reduces in parallel along the
  * key/value dimension).
  *
- * n_splits: 0 = automatic (about two CTAs per SM); otherwise the requested
+ * n_splits: 0 = automatic (the largest count that keeps all B * Hkv * n_splits
+ * CTAs in one wave on the GPU's 152 SMs, at least 1); otherwise the requested
  * number of ranges, reduced so that no range is empty (at most ceil(Skv/128)).
  * workspace: caller-owned device memory of at least
  * fa_fwd_splitkv_workspace_bytes(...) bytes, 256-byte aligned, for the

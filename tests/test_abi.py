@@ -183,7 +183,7 @@ def test_splitkv_workspace_plan(fa_lib):
 
     def expect(B, Hq, Hkv, Sq, Skv, d, n_req):
         tiles = (Skv + 127) // 128
-        want = n_req if n_req > 0 else -(-2 * 152 // (B * Hkv))
+        want = n_req if n_req > 0 else 152 // (B * Hkv)
         want = max(1, min(want, tiles))
         per = -(-tiles // want)
         n = -(-tiles // per)
