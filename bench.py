@@ -247,6 +247,9 @@ def run_gpu(args, w, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     q, k, v, do = fa_inputs.make_inputs(w)
+    if w.page_size:   # K and V become the paged caches (block table on the device)
+        k, v, table, _ = fa_inputs.make_paged(k, v, w.page_size, seed=w.page_size)
+        tables = [table.to(dev), table.to(dev)]
     qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
     out = torch.empty_like(qd)
     lse = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
@@ -264,8 +267,13 @@ def run_gpu(args, w, rank, world, local_rank):
 
         def fwd_call(q_, k_, v_, o_, l_, causal, scale, st, _ws=dec_ws):
             ws_ = _ws[1] if (q_.data_ptr() != qd.data_ptr()) else _ws[0]
-            fa.fa_fwd_splitkv(q_, k_, v_, o_, l_, causal, scale, 0,
-                              ws_ if dec_ws_bytes else None, st)
+            if w.page_size:   # k_, v_ are the paged caches; the block table rides along
+                fa.fa_fwd_splitkv_paged(q_, k_, v_, tables[0 if q_.data_ptr() == qd.data_ptr() else 1],
+                                        o_, l_, w.kv_len, causal, scale, 0,
+                                        ws_ if dec_ws_bytes else None, st)
+            else:
+                fa.fa_fwd_splitkv(q_, k_, v_, o_, l_, causal, scale, 0,
+                                  ws_ if dec_ws_bytes else None, st)
 
     def step():
         fwd_call(qd, kd, vd, out, lse, w.causal, w.scale, stream)

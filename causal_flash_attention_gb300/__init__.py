@@ -3,7 +3,7 @@ libfa (include/fa.h).
 
 The functions with the C names (`fa_fwd`, `fa_bwd`, `fa_bwd_workspace_bytes`,
 `fa_fwd_kv`, `fa_bwd_kv`, `fa_bwd_kv_workspace_bytes`, `fa_fwd_splitkv`,
-`fa_fwd_splitkv_workspace_bytes`, `fa_strerror`,
+`fa_fwd_splitkv_workspace_bytes`, `fa_fwd_splitkv_paged`, `fa_strerror`,
 `fa_last_device_status`, `fa_version`) only marshal arguments:
 shapes come from the tensors, pointers from `data_ptr()`, and the stream from
 PyTorch's current stream. Every step of the computation runs in libfa's CUDA
@@ -27,7 +27,7 @@ __all__ = [
     "fa_last_device_status", "fa_version", "attention_forward", "attention_backward",
     "DTYPE_CODES", "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_fwd_kv", "fa_bwd_kv",
     "fa_bwd_kv_workspace_bytes", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes",
-    "decode_forward",
+    "decode_forward", "fa_fwd_splitkv_paged", "decode_forward_paged",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
     L.fa_fwd_splitkv.restype = i32
     L.fa_fwd_splitkv_workspace_bytes.argtypes = [i32] * 7
     L.fa_fwd_splitkv_workspace_bytes.restype = sz
+    L.fa_fwd_splitkv_paged.argtypes = [vp] * 6 + [i32] * 10 + [f32, i32, i32, vp, sz, vp]
+    L.fa_fwd_splitkv_paged.restype = i32
     L.fa_strerror.argtypes = [i32]
     L.fa_strerror.restype = ctypes.c_char_p
     L.fa_last_device_status.argtypes = [vp, ctypes.POINTER(i32)]
@@ -211,6 +213,43 @@ def decode_forward(q, k, v, causal=True, scale=None, n_splits=0, stream=None):
     n = fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d, n_splits)
     ws = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
     fa_fwd_splitkv(q, k, v, out, lse, causal, scale, n_splits, ws, stream)
+    return out, lse
+
+
+def fa_fwd_splitkv_paged(q, k_cache, v_cache, block_table, out, lse, Skv, causal=True,
+                         scale=None, n_splits=0, workspace=None, stream=None):
+    """Call fa_fwd_splitkv_paged: q [B,Hq,Sq,d]; k_cache/v_cache
+    [num_blocks,Hkv,block_size,d]; block_table int32 [B,max_blocks]; every
+    sequence holds Skv keys."""
+    _check_contig(q, k_cache, v_cache, block_table, out, lse)
+    if q.dim() != 4 or k_cache.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("q [B,Hq,Sq,d], caches [num_blocks,Hkv,block_size,d], table [B,max_blocks]")
+    if block_table.dtype != torch.int32:
+        raise ValueError("block_table must be int32")
+    B, Hq, Sq, d = (int(x) for x in q.shape)
+    num_blocks, Hkv, block_size = (int(x) for x in k_cache.shape[:3])
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().fa_fwd_splitkv_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(out), _ptr(lse), B, Hq,
+        Hkv, Sq, int(Skv), d, block_size, num_blocks, int(block_table.shape[1]),
+        int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), int(n_splits), _ptr(workspace),
+        ws_bytes, _stream(stream))
+    if rc != 0:
+        raise FAError(rc, "fa_fwd_splitkv_paged")
+
+
+def decode_forward_paged(q, k_cache, v_cache, block_table, Skv, causal=True, scale=None,
+                         n_splits=0, stream=None):
+    """Allocate out, lse and the split workspace and run fa_fwd_splitkv_paged."""
+    B, Hq, Sq, d = (int(x) for x in q.shape)
+    Hkv = int(k_cache.shape[1])
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    n = fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, Sq, int(Skv), d, n_splits)
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    fa_fwd_splitkv_paged(q, k_cache, v_cache, block_table, out, lse, Skv, causal, scale, n_splits,
+                         ws, stream)
     return out, lse
 
 

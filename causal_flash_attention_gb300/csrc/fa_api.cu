@@ -46,13 +46,14 @@ int* status_ptr() {
 
 // 3-D view [rows = BH][S][d] of a contiguous 16-bit tensor; box = 64 columns
 // (128 bytes, one swizzle span) x 128 sequence rows x 1 head.
-bool make_tmap(CUtensorMap* m, const void* base, int BH, int S, int d, bool bf16) {
+bool make_tmap(CUtensorMap* m, const void* base, int BH, int S, int d, bool bf16,
+               int box_rows = kTileM) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(S) * d * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(kTileM), 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kChunk), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -324,18 +325,17 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, i
   return split_plan(B, Hq, Hkv, Sq, Skv, d, n_splits).total;
 }
 
-int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
-                   int Hq, int Hkv, int Sq, int Skv, int d, int causal, float scale, int dtype,
-                   int n_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
-  if (rc != FA_OK) return rc;
-  if (n_splits < 0 || (Hq / Hkv) * Sq > kDecodeMaxRows) return FA_ERR_SHAPE;
-  if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
-    return FA_ERR_ALIGN;
-  if (dtype == FA_F32)   // plain fp32 arithmetic: one warp per query row, no split
-    return fa_fwd_kv(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype, stream);
+}  // extern "C"
 
+namespace {
+
+// Shared body of fa_fwd_splitkv and fa_fwd_splitkv_paged (block_table null:
+// contiguous K/V).
+int splitkv_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                 int Hkv, int Sq, int Skv, int d, int causal, float scale, int dtype, int n_splits,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream,
+                 const int* block_table, int block_size, int max_blocks, int num_blocks) {
+  const bool paged = block_table != nullptr;
   const SplitPlan sp = split_plan(B, Hq, Hkv, Sq, Skv, d, n_splits);
   if (sp.total > 0 && (!workspace || workspace_bytes < sp.total)) return FA_ERR_WORKSPACE;
   if (sp.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
@@ -345,8 +345,19 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float
 
   DecodeParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16))
+  if (paged) {
+    p.box_rows = std::min(block_size, kTileN);
+    if (!make_tmap(&p.tm_k, k, num_blocks * Hkv, block_size, d, bf16, p.box_rows) ||
+        !make_tmap(&p.tm_v, v, num_blocks * Hkv, block_size, d, bf16, p.box_rows))
+      return FA_ERR_TMA;
+    p.block_table = block_table;
+    p.block_size = block_size;
+    p.max_blocks = max_blocks;
+    p.num_blocks = num_blocks;
+  } else if (!make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
+             !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16)) {
     return FA_ERR_TMA;
+  }
   p.q = q;
   p.out = out;
   p.lse = lse;
@@ -375,6 +386,47 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float
   m.n_splits = sp.n_splits;
   m.dtype = dtype;
   return launch_decode_merge(m, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Skv, int d, int causal, float scale, int dtype,
+                   int n_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (n_splits < 0 || (Hq / Hkv) * Sq > kDecodeMaxRows) return FA_ERR_SHAPE;
+  if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if (dtype == FA_F32)   // plain fp32 arithmetic: one warp per query row, no split
+    return fa_fwd_kv(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype, stream);
+  return splitkv_impl(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype, n_splits,
+                      workspace, workspace_bytes, stream, nullptr, 0, 0, 0);
+}
+
+int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
+                         const int* block_table, void* out, float* lse, int B, int Hq, int Hkv,
+                         int Sq, int Skv, int d, int block_size, int num_blocks, int max_blocks,
+                         int causal, float scale, int dtype, int n_splits, void* workspace,
+                         size_t workspace_bytes, fa_stream_t stream) {
+  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (dtype == FA_F32) return FA_ERR_DTYPE;   // the paged path runs on the tensor cores only
+  if (n_splits < 0 || (Hq / Hkv) * Sq > kDecodeMaxRows) return FA_ERR_SHAPE;
+  if (block_size < 16 || block_size > 1024 || (block_size & (block_size - 1)) != 0 ||
+      num_blocks < 1 || static_cast<long long>(num_blocks) * Hkv > (1LL << 30) ||
+      max_blocks < (Skv + block_size - 1) / block_size)
+    return FA_ERR_SHAPE;
+  if (!q || !k_cache || !v_cache || !block_table || !out || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(lse) || (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+    return FA_ERR_ALIGN;
+  return splitkv_impl(q, k_cache, v_cache, out, lse, B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype,
+                      n_splits, workspace, workspace_bytes, stream, block_table, block_size,
+                      max_blocks, num_blocks);
 }
 
 int fa_last_device_status(fa_stream_t stream, int* status) {

@@ -140,35 +140,69 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (warp == 0) {
     // ===================== TMA producer =====================
+    // Lane 0 waits for a free slot and posts the expected bytes. Contiguous:
+    // lane 0 then issues the tile's one box per 64-column chunk. Paged: each
+    // lane i < 128 / box_rows reads the block-table entry of box i and issues
+    // that box itself, so that the boxes of a tile are issued in parallel and
+    // no copy waits on a dependent table load.
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      int j = 0;
-      for (; j < n; ++j) {
-        const int st = j % NS;
-        const uint32_t use = static_cast<uint32_t>(j / NS);
-        const int row = (t_begin + j) * kTileN;
-        if (j >= NS && !mbar_wait(k_empty(st), (use - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(k_full(st), Cfg::kTileBytes);
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_3d(sbase + Cfg::kOffK + st * Cfg::kTileBytes + c * (kTileN * 128), &p.tm_k,
-                      k_full(st), c * kChunk, row, bkv);
-        if (j >= NS && !mbar_wait(v_empty(st), (use - 1) & 1, abort_flag, p.status)) {
-          ++j;   // this round's K load is in flight
-          break;
-        }
-        mbar_arrive_expect_tx(v_full(st), Cfg::kTileBytes);
-        for (int c = 0; c < Cfg::kChunks; ++c)
-          tma_load_3d(sbase + Cfg::kOffV + st * Cfg::kTileBytes + c * (kTileN * 128), &p.tm_v,
-                      v_full(st), c * kChunk, row, bkv);
+    }
+    const int n_blocks = p.block_table ? (p.Skv + p.block_size - 1) / p.block_size : 0;
+    const int n_boxes = p.block_table ? kTileN / p.box_rows : 1;
+    // This lane's part of one 128-key tile into `dst` (chunk c at dst + c *
+    // 16 KB). Paged: a block past the sequence, or a table entry outside
+    // [0, num_blocks), is loaded from an out-of-range row, which the copy
+    // fills with zeros.
+    auto load_part = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int tile, int pb) {
+      if (!p.block_table) {
+        if (lane == 0)
+          for (int c = 0; c < Cfg::kChunks; ++c)
+            tma_load_3d(dst + c * (kTileN * 128), tm, bar, c * kChunk, tile * kTileN, bkv);
+        return;
       }
-      if (*abort_flag) {
-        // let every copy already issued land before the CTA releases its memory
-        for (int jj = max(0, j - NS); jj < j; ++jj) {
-          const uint32_t par = static_cast<uint32_t>(jj / NS) & 1;
-          drain_wait_d(k_full(jj % NS), par, p.status);
-          drain_wait_d(v_full(jj % NS), par, p.status);
-        }
+      if (lane >= n_boxes) return;
+      const int key = tile * kTileN + lane * p.box_rows;
+      const bool in_range = pb >= 0 && pb < p.num_blocks;
+      const int y = in_range ? key % p.block_size : p.block_size;   // out of range: zeros
+      const int z = in_range ? pb * p.Hkv + kvh : 0;
+      for (int c = 0; c < Cfg::kChunks; ++c)
+        tma_load_3d(dst + c * (kTileN * 128) + lane * p.box_rows * 128, tm, bar, c * kChunk, y, z);
+    };
+    int j = 0;
+    for (; j < n; ++j) {
+      const int tile = t_begin + j;
+      const int st = j % NS;
+      const uint32_t use = static_cast<uint32_t>(j / NS);
+      int pb = -1;
+      if (p.block_table && lane < n_boxes) {
+        const int lb = (tile * kTileN + lane * p.box_rows) / p.block_size;
+        if (lb < n_blocks) pb = p.block_table[static_cast<size_t>(b) * p.max_blocks + lb];
+      }
+      int stop = 0;
+      if (lane == 0) {
+        if (j >= NS && !mbar_wait(k_empty(st), (use - 1) & 1, abort_flag, p.status)) stop = 1;
+        else mbar_arrive_expect_tx(k_full(st), Cfg::kTileBytes);
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      load_part(&p.tm_k, sbase + Cfg::kOffK + st * Cfg::kTileBytes, k_full(st), tile, pb);
+      if (lane == 0) {
+        if (j >= NS && !mbar_wait(v_empty(st), (use - 1) & 1, abort_flag, p.status)) stop = 1;
+        else mbar_arrive_expect_tx(v_full(st), Cfg::kTileBytes);
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) {
+        ++j;   // this round's K load is in flight
+        break;
+      }
+      load_part(&p.tm_v, sbase + Cfg::kOffV + st * Cfg::kTileBytes, v_full(st), tile, pb);
+    }
+    if (lane == 0 && *abort_flag) {
+      // let every copy already issued land before the CTA releases its memory
+      for (int jj = max(0, j - NS); jj < j; ++jj) {
+        const uint32_t par = static_cast<uint32_t>(jj / NS) & 1;
+        drain_wait_d(k_full(jj % NS), par, p.status);
+        drain_wait_d(v_full(jj % NS), par, p.status);
       }
     }
   } else if (warp == 1) {

@@ -11,8 +11,8 @@ namespace fa {
 // query tile packs the R = G * Sq query rows of the head's G query heads
 // (row r = gq * Sq + s for query head kvh * G + gq and query row s).
 struct DecodeParams {
-  CUtensorMap tm_k;   // [B*Hkv][Skv][d], box (64, 128, 1), 128B swizzle
-  CUtensorMap tm_v;
+  CUtensorMap tm_k;   // contiguous: [B*Hkv][Skv][d], box (64, 128, 1), 128B swizzle;
+  CUtensorMap tm_v;   // paged: [num_blocks*Hkv][block_size][d], box (64, box_rows, 1)
   const void* q;      // [B*Hq][Sq][d]
   void* out;          // [B*Hq][Sq][d]   written when n_splits == 1
   float* lse;         // [B*Hq][Sq]      written when n_splits == 1
@@ -24,6 +24,12 @@ struct DecodeParams {
   int tiles_per_split, n_splits;
   float scale_log2;   // softmax scale * log2(e)
   int* status;
+  // Paged key/value cache (block_table != nullptr): key position t of batch b
+  // is row t % block_size of physical block block_table[b * max_blocks +
+  // t / block_size]; a 128-key tile is loaded as 128 / box_rows boxes
+  // (box_rows = min(block_size, 128)).
+  const int* block_table;
+  int block_size, box_rows, max_blocks, num_blocks;
 };
 
 struct DecodeMergeParams {

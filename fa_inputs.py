@@ -23,6 +23,8 @@ Workloads (shapes in [B, H, S, d] order, Q/dO with Hq heads, K/V with Hkv):
                forward only: one new token per sequence over an 8192-key cache
   spec_32k     bf16,  B=2 Hq=32 Hkv=8 Sq=4 Skv=32768 d=128, N(0,1), seed 7,
                forward only: four new tokens over a 32768-key cache
+  decode_8k_paged  decode_8k with its cache in 64-key blocks at seeded random
+               places of a shared pool (make_paged, seed 64)
 
 All use scale = 1/sqrt(d); all but the *_nc workloads use causal masking.
 S is the query length; K and V have `kv_len` rows (S unless Skv is given).
@@ -54,6 +56,7 @@ class Workload:
     spike_scale: float = 1.0      # ... are multiplied by this before rounding
     Skv: int = 0                  # key/value length; 0 means the same as S
     decode: bool = False          # few query rows: timed through the split-KV forward
+    page_size: int = 0            # > 0: K/V in a paged cache of blocks of this many keys
 
     @property
     def kv_len(self) -> int:
@@ -95,6 +98,8 @@ WORKLOADS = {
                  decode=True),
         Workload("spec_32k", "bf16", 2, 32, 8, 4, 128, seed=7, Skv=32768, backward=False,
                  decode=True),
+        Workload("decode_8k_paged", "bf16", 16, 32, 8, 1, 128, seed=6, Skv=8192,
+                 backward=False, decode=True, page_size=64),
     ]
 }
 
@@ -135,6 +140,34 @@ def make_custom(B, Hq, Hkv, S, d, dtype="bf16", seed=0, value_scale=1.0,
     w = Workload("custom", dtype, B, Hq, Hkv, S, d, seed=seed,
                  value_scale=value_scale, Skv=Skv)
     return make_inputs(w, with_dout=with_dout)
+
+
+def make_paged(k, v, block_size: int, seed: int, spare_blocks: int = 3):
+    """Scatter contiguous k, v [B, Hkv, Skv, d] into a paged cache.
+
+    Returns (k_cache, v_cache, block_table, num_blocks): caches
+    [num_blocks, Hkv, block_size, d] with the sequences' blocks at seeded random
+    physical positions (plus `spare_blocks` unused blocks filled with large
+    values that must never be read), and an int32 block table [B, max_blocks]
+    whose entries past each sequence's last block are -1. A layout change only:
+    no attention arithmetic.
+    """
+    B, Hkv, Skv, d = k.shape
+    per_seq = -(-Skv // block_size)
+    num_blocks = B * per_seq + spare_blocks
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_blocks, generator=g)
+    table = torch.full((B, per_seq + 2), -1, dtype=torch.int32)
+    k_cache = torch.full((num_blocks, Hkv, block_size, d), 1000.0, dtype=k.dtype)
+    v_cache = torch.full((num_blocks, Hkv, block_size, d), 1000.0, dtype=v.dtype)
+    for b in range(B):
+        for lb in range(per_seq):
+            pb = int(perm[b * per_seq + lb])
+            table[b, lb] = pb
+            t0, t1 = lb * block_size, min((lb + 1) * block_size, Skv)
+            k_cache[pb, :, : t1 - t0] = k[b, :, t0:t1]
+            v_cache[pb, :, : t1 - t0] = v[b, :, t0:t1]
+    return k_cache, v_cache, table, num_blocks
 
 
 def sample_rows(S: int, n: int, seed: int, tile: int = 128):

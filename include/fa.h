@@ -169,6 +169,30 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, i
                                       int n_splits);
 
 /*
+ * fa_fwd_splitkv over a paged key/value cache: the keys and values of all
+ * sequences live in fixed-size blocks of a shared pool, and a block table maps
+ * each sequence's logical blocks to physical ones ("Flash Attention" glossary
+ * page, section 与 PagedAttention、KV Cache 的组合: a paged decode kernel looks
+ * up the block table while it loads the K/V tiles and runs the online
+ * softmax). Layouts:
+ *   k_cache, v_cache : [num_blocks][Hkv][block_size][d]   (dtype)
+ *   block_table      : [B][max_blocks] int32; key position t of sequence b is
+ *                      row t % block_size of block block_table[b][t / block_size]
+ * block_size: a power of two from 16 to 1024. Only the first
+ * ceil(Skv / block_size) entries of a row are read (max_blocks must be at
+ * least that); an entry outside [0, num_blocks) reads as zeros instead of
+ * faulting. Every sequence has the same Skv. q, out, lse, the mask, the
+ * results, n_splits and the workspace (fa_fwd_splitkv_workspace_bytes) are as
+ * for fa_fwd_splitkv. FA_BF16 and FA_F16 only (FA_F32 gives FA_ERR_DTYPE).
+ */
+int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
+                         const int* block_table, void* out, float* lse,
+                         int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                         int block_size, int num_blocks, int max_blocks, int causal,
+                         float scale, int dtype, int n_splits, void* workspace,
+                         size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Size of the fixed device scratch array behind fa_bwd_noalloc (32 MiB). A
  * call fits when fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) is at most this,
  * e.g. B*Hq = 96 heads at S = 1024, d = 64 (about 25.9 MB).

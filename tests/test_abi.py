@@ -198,3 +198,24 @@ def test_splitkv_workspace_plan(fa_lib):
     assert ws(1, 8, 2, 1, 4096, 128, 0) > 0
     assert ws(1, 2, 2, 1, 128, 128, 0) == 0          # one key tile: one range, no workspace
     assert ws(1, 16, 4, 33, 4096, 128, 0) == 0       # invalid: G * Sq > 128
+
+
+def _paged(L, q=16, kc=16, vc=16, table=16, out=16, lse=16, B=2, Hq=8, Hkv=2, Sq=1, Skv=1000,
+           d=128, block_size=64, num_blocks=40, max_blocks=16, causal=1, scale=0.125, dtype=2,
+           n_splits=0, ws=256, ws_bytes=1 << 30):
+    return L.fa_fwd_splitkv_paged(q, kc, vc, table, out, lse, B, Hq, Hkv, Sq, Skv, d, block_size,
+                                  num_blocks, max_blocks, causal, scale, dtype, n_splits, ws,
+                                  ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(block_size=8), FA_ERR_SHAPE), (dict(block_size=48), FA_ERR_SHAPE),
+    (dict(block_size=2048), FA_ERR_SHAPE), (dict(num_blocks=0), FA_ERR_SHAPE),
+    (dict(max_blocks=15), FA_ERR_SHAPE),             # ceil(1000 / 64) = 16 entries needed
+    (dict(max_blocks=16, table=None), FA_ERR_NULL), (dict(table=18), FA_ERR_ALIGN),
+    (dict(kc=None), FA_ERR_NULL), (dict(vc=8), FA_ERR_ALIGN), (dict(dtype=0), FA_ERR_DTYPE),
+    (dict(Sq=33, Hq=16, Hkv=4), FA_ERR_SHAPE), (dict(Sq=2000), FA_ERR_SHAPE),
+    (dict(block_size=1024, max_blocks=1, q=None), FA_ERR_NULL),
+])
+def test_paged_rejects_bad_arguments(fa_lib, kw, code):
+    assert _paged(fa_lib.lib(), **kw) == code

@@ -78,3 +78,62 @@ def test_decode_workload(fa, name):
     got = run_decode(fa, q, k, v, w.causal, w.scale, 0)
     out_ref, lse_ref = oracle.forward(*map(f64, (q, k, v)), w.causal, w.scale)
     check_fwd(got, out_ref, lse_ref)
+
+
+# ------------------------------------------------------- paged key/value --
+PAGED = [
+    # B, Hq, Hkv, Sq, Skv, d, dtype, causal, block_size, n_splits
+    (2, 8, 2, 1, 1000, 128, "bf16", True, 16, 0),
+    (3, 4, 4, 2, 777, 64, "fp16", True, 32, 3),
+    (1, 8, 1, 16, 4096, 128, "bf16", True, 64, 0),
+    (2, 4, 2, 1, 300, 128, "bf16", False, 128, 0),
+    (2, 8, 2, 4, 2500, 128, "bf16", True, 256, 2),
+    (1, 2, 1, 1, 5000, 128, "bf16", True, 1024, 0),
+]
+
+
+def run_paged(fa, q, k, v, causal, scale, block_size, n_splits, seed):
+    dev = torch.device("cuda", 0)
+    kc, vc, table, _ = fa_inputs.make_paged(k, v, block_size, seed)
+    qd, kcd, vcd, td = (x.to(dev) for x in (q, kc, vc, table))
+    out, lse = fa.decode_forward_paged(qd, kcd, vcd, td, k.shape[2], causal, scale, n_splits)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    return {"out": f64(out), "lse": f64(lse)}
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Skv,d,dtype,causal,block_size,n_splits", PAGED)
+def test_decode_paged(fa, B, Hq, Hkv, Sq, Skv, d, dtype, causal, block_size, n_splits):
+    """The paged cache holds the same keys and values at scattered blocks
+    (unused rows and blocks hold 1000.0, which must never be read)."""
+    q, k, v, _ = fa_inputs.make_custom(B, Hq, Hkv, Sq, d, dtype, seed=Skv + block_size, Skv=Skv)
+    scale = 1.0 / np.sqrt(d)
+    got = run_paged(fa, q, k, v, causal, scale, block_size, n_splits, seed=block_size)
+    out_ref, lse_ref = oracle.forward(*map(f64, (q, k, v)), causal, scale)
+    check_fwd(got, out_ref, lse_ref)
+
+
+def test_decode_paged_out_of_range_entries_read_zeros(fa):
+    """A block-table entry outside [0, num_blocks) reads as a zero block: the
+    result equals the oracle on K and V with those positions zeroed."""
+    dev = torch.device("cuda", 0)
+    q, k, v, _ = fa_inputs.make_custom(1, 4, 2, 1, 128, "bf16", seed=3, Skv=512)
+    kc, vc, table, nb = fa_inputs.make_paged(k, v, 64, seed=4)
+    table[0, 2] = nb + 5          # keys 128..191 read as zeros
+    k0, v0 = k.clone(), v.clone()
+    k0[:, :, 128:192] = 0
+    v0[:, :, 128:192] = 0
+    qd, kcd, vcd, td = (x.to(dev) for x in (q, kc, vc, table))
+    out, lse = fa.decode_forward_paged(qd, kcd, vcd, td, 512, True, 1 / np.sqrt(128))
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    ref = oracle.forward(*map(f64, (q, k0, v0)), True, 1 / np.sqrt(128))
+    check_fwd({"out": f64(out), "lse": f64(lse)}, *ref)
+
+
+def test_decode_paged_workload(fa):
+    w = fa_inputs.WORKLOADS["decode_8k_paged"]
+    q, k, v = fa_inputs.make_inputs(w, with_dout=False)
+    got = run_paged(fa, q, k, v, w.causal, w.scale, w.page_size, 0, seed=w.page_size)
+    out_ref, lse_ref = oracle.forward(*map(f64, (q, k, v)), w.causal, w.scale)
+    check_fwd(got, out_ref, lse_ref)
