@@ -137,6 +137,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the merge kernel (when there is one) may be scheduled now; it waits for
+  // this grid's completion before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ===================== TMA producer =====================
@@ -431,9 +434,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 // ------------------------------------------------------------------ merge --
-// One warp per output row (b, hq, s); each lane combines d / 32 columns.
+// One warp per output row (b, hq, s). The lanes first read the ranges'
+// lse2 in parallel (lane i: ranges i, i + 32, ...) and reduce M and the
+// weights with shuffles; then each lane combines d / 32 columns of the
+// ranges' partial rows, four ranges' loads in flight at a time.
 template <typename T, int PER>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeMergeParams p) {
+  // Launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partial results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // (b * Hq + hq) * Sq + s
   if (row >= static_cast<long long>(p.B) * p.Hq * p.Sq) return;
@@ -444,19 +453,29 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeMergePara
   const int r = (hq % p.G) * p.Sq + s;
   const size_t base = static_cast<size_t>(bkv) * p.n_splits;
   float M = -INFINITY;
-  for (int sp = 0; sp < p.n_splits; ++sp) M = fmaxf(M, p.part_lse2[(base + sp) * p.R + r]);
+  for (int sp = lane; sp < p.n_splits; sp += 32) M = fmaxf(M, p.part_lse2[(base + sp) * p.R + r]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
-  for (int sp = 0; sp < p.n_splits; ++sp) {
-    const size_t prow = (base + sp) * p.R + r;
-    const float w = (M == -INFINITY) ? 0.f : ex2(p.part_lse2[prow] - M);
-    L += w;
-    const float* src = p.part_out + prow * p.d + lane * PER;
+  for (int sp0 = 0; sp0 < p.n_splits; sp0 += 32) {
+    const int sp = sp0 + lane;
+    const float wl = (sp < p.n_splits && M != -INFINITY) ? ex2(p.part_lse2[(base + sp) * p.R + r] - M)
+                                                          : 0.f;
+    L += wl;
+    const int cnt = min(32, p.n_splits - sp0);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, wl, k);
+      const float* src = p.part_out + ((base + sp0 + k) * p.R + r) * p.d + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, src[e], acc[e]);
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   T* dst = static_cast<T*>(p.out) + row * p.d + lane * PER;
 #pragma unroll
@@ -483,17 +502,25 @@ cudaError_t launch_decode(const DecodeParams& p, int d, bool bf16, cudaStream_t 
   return bf16 ? launch_decode_impl<64, true>(p, stream) : launch_decode_impl<64, false>(p, stream);
 }
 
+// The merge runs as a programmatic dependent launch of the split kernel on the
+// same stream, so that its launch overlaps the split kernel's tail.
 cudaError_t launch_decode_merge(const DecodeMergeParams& p, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
-  if (p.dtype == 2) {
-    if (p.d == 128) decode_merge_kernel<__nv_bfloat16, 4><<<grid, 256, 0, stream>>>(p);
-    else decode_merge_kernel<__nv_bfloat16, 2><<<grid, 256, 0, stream>>>(p);
-  } else {
-    if (p.d == 128) decode_merge_kernel<__half, 4><<<grid, 256, 0, stream>>>(p);
-    else decode_merge_kernel<__half, 2><<<grid, 256, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.dtype == 2)
+    return p.d == 128 ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<__nv_bfloat16, 4>, p)
+                      : cudaLaunchKernelEx(&cfg, decode_merge_kernel<__nv_bfloat16, 2>, p);
+  return p.d == 128 ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<__half, 4>, p)
+                    : cudaLaunchKernelEx(&cfg, decode_merge_kernel<__half, 2>, p);
 }
 
 }  // namespace fa
