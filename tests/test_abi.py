@@ -1,7 +1,6 @@
 """The C ABI without a GPU: the library loads, exports every function that
 include/fa.h declares, and rejects bad arguments on the host with the
 documented codes before touching the device."""
-import ctypes
 import os
 import re
 

@@ -17,7 +17,7 @@ import torch
 
 import fa_inputs
 import oracle
-from parity import LSE_TOL, OUT_TOL, check_fwd, f64
+from parity import check_fwd, f64
 
 pytestmark = pytest.mark.gpu
 

@@ -3,10 +3,10 @@ against the fp64 oracle, with the causal mask aligned to the last key: query
 row i stands at position i + (Skv - Sq) ("Phase 14: Flash Attention 2 for
 SM120", section Causal Mask, kv_offset = kv_len - q_len).
 
-Same bars as the self-attention parity tests (tests/parity.py). Edge shapes put the diagonal at offsets that
-are and are not multiples of the 128-key tile (so the masked band spans one or
-two key tiles), single-query rows, and unmasked calls with fewer keys than
-queries. Full size: prefill_8k (a 2048-query chunk over 8192 keys, GQA 32/8)
+Same bars as the self-attention parity tests (tests/parity.py). Edge shapes
+put the diagonal at offsets that are and are not multiples of the 128-key tile
+(so the masked band spans one or two key tiles), single-query rows, and
+unmasked calls with fewer keys than queries. Full size: prefill_8k (a 2048-query chunk over 8192 keys, GQA 32/8)
 and the unmasked long_8k_nc / gqa_qwen3_nc, in the launch configuration the
 benchmark times.
 """
@@ -77,7 +77,7 @@ def test_kv_entry_with_equal_lengths_is_the_self_attention_call(fa):
     assert fa.fa_last_device_status() == 0
     for a, b in zip(outs[0][:2] + outs[0][3:], outs[1][:2] + outs[1][3:]):
         assert torch.equal(a, b)
-    check_grad("dq", f64(outs[1][2]), f64(outs[0][2]).astype(np.float64))
+    check_grad("dq", f64(outs[1][2]), f64(outs[0][2]))
 
 
 def test_causal_with_fewer_keys_is_rejected(fa):
