@@ -232,6 +232,23 @@ def oracle_sample(w, head_inputs, block):
     return dt, (14 if w.backward else 4) * visible_pairs(r, kv, w.causal) * w.d
 
 
+# ------------------------------------------------------------ multi-rank --
+def max_over_ranks(times, dist, device):
+    """Each timing's maximum over all ranks (the slowest rank sets the job's
+    time); `dist` None means a single process."""
+    import torch
+    t = torch.tensor(times, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(flops_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: every rank's FLOPs per step over the slowest
+    rank's step time (weak scaling: each rank runs its own replica)."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- GPU arm --
 def run_gpu(args, w, rank, world, local_rank):
     import torch
@@ -381,10 +398,7 @@ def run_gpu(args, w, rank, world, local_rank):
     if status:
         raise RuntimeError(f"device status {status} in the timed region")
 
-    t = torch.tensor([total_ms, fwd_ms, bwd_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, fwd_ms, bwd_ms, e2e_ms = t.tolist()
+    total_ms, fwd_ms, bwd_ms, e2e_ms = max_over_ranks([total_ms, fwd_ms, bwd_ms, e2e_ms], dist, dev)
     return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, clocks=clocks.summary(), dist=dist,
                 launches_per_fwd=(2 if dec_ws_bytes else 1))
@@ -465,11 +479,10 @@ def main():
         return
     K = args.steps
     ms_per_step = r["total_ms"] / K
-    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(step_flops, world, ms_per_step)
     fwd_tf = flops(w, True, False) / (r["fwd_ms"] * 1e-3) / 1e12
     bwd_tf = flops(w, False, True) / (r["bwd_ms"] * 1e-3) / 1e12 if w.backward else None
-    e2e_tf = (step_flops * world / (r["e2e_ms"] * 1e-3) / 1e12) if r["e2e_ms"] == r["e2e_ms"] \
-        else None
+    e2e_tf = job_tflops(step_flops, world, r["e2e_ms"]) if r["e2e_ms"] == r["e2e_ms"] else None
     peak = peaks["bf16_tflops"]
     traffic = recorded_traffic("fa_bwd_kernel", w.name)
     if args.heads:
