@@ -98,10 +98,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   const int bh = static_cast<int>(row / p.Sq_pad), i = static_cast<int>(row % p.Sq_pad);
   float dsum = 0.f;
   if (i < p.Sq) {
+    // d / 32 (2 or 4) consecutive elements per lane, one vector load each
     const size_t off = (static_cast<size_t>(bh) * p.Sq + i) * p.d;
     const T* o = static_cast<const T*>(p.out) + off;
     const T* g = static_cast<const T*>(p.dout) + off;
-    for (int e = lane; e < p.d; e += 32) dsum = fmaf(to_f(o[e]), to_f(g[e]), dsum);
+    const int per = p.d / 32;
+    if (per == 4) {
+      struct alignas(4 * sizeof(T)) V4 { T x[4]; };
+      const V4 ov = reinterpret_cast<const V4*>(o)[lane], gv = reinterpret_cast<const V4*>(g)[lane];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dsum = fmaf(to_f(ov.x[e]), to_f(gv.x[e]), dsum);
+    } else {
+      struct alignas(2 * sizeof(T)) V2 { T x[2]; };
+      const V2 ov = reinterpret_cast<const V2*>(o)[lane], gv = reinterpret_cast<const V2*>(g)[lane];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) dsum = fmaf(to_f(ov.x[e]), to_f(gv.x[e]), dsum);
+    }
   }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
