@@ -171,9 +171,9 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, i
 /*
  * fa_fwd_splitkv over a paged key/value cache: the keys and values of all
  * sequences live in fixed-size blocks of a shared pool, and a block table maps
- * each sequence's logical blocks to physical ones ("Flash Attention" glossary
- * page, section 与 PagedAttention、KV Cache 的组合: a paged decode kernel looks
- * up the block table while it loads the K/V tiles and runs the online
+ * each sequence's logical blocks to physical ones ("FlashAttention 与 SDPA
+ * Backend", section 与 PagedAttention、KV Cache 的组合: a paged decode kernel
+ * looks up the block table while it loads the K/V tiles and runs the online
  * softmax). Layouts:
  *   k_cache, v_cache : [num_blocks][Hkv][block_size][d]   (dtype)
  *   block_table      : [B][max_blocks] int32; key position t of sequence b is
