@@ -62,6 +62,22 @@ bool make_tmap(CUtensorMap* m, const void* base, int BH, int S, int d, bool bf16
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view [BH][S_pad][d] of the fp32 dQ accumulator for bulk reduce-adds;
+// box = 32 columns (128 bytes) x 32 rows x 1 head, no swizzle.
+bool make_tmap_acc(CUtensorMap* m, float* base, int BH, int S_pad, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(S_pad),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(S_pad) * d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Sq query rows against Skv key/value rows. Under the causal mask query row i
@@ -281,7 +297,8 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
   if (!make_tmap(&p.tm_q, q, BH, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
-      !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16))
+      !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16) ||
+      (d == 128 && !make_tmap_acc(&p.tm_dq, pre.dq_acc, BH, Sq_pad, d)))
     return FA_ERR_TMA;
   p.delta = pre.delta;
   p.lse2 = pre.lse2;

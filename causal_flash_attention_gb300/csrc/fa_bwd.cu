@@ -22,12 +22,16 @@
 //                     16-bit into TMEM; dS^T = P^T (dP^T - D) written to smem]
 //                    dV  += P^T dO_i           (P^T from TMEM)
 //                    dK  += dS^T Q_i
-//                    dQ   = dS K_j             -> TMEM, then added (fp32 vector
-//                                                 atomics) into the dQ accumulator
+//                    dQ   = dS K_j             -> TMEM, then added into the fp32
+//                                                 dQ accumulator (d = 128: bulk
+//                                                 tensor reduce-adds of boxes staged
+//                                                 in shared memory; d = 64: 16-byte
+//                                                 vector atomics)
 //   3. dq_convert: dq = scale * accumulator, rounded to the input type.
 //
 // Warp roles of bwd_main (320 threads): warp 0 TMA producer (K_j, V_j once;
-// Q_i, dO_i, L_i, D_i through a 2-stage ring), warp 1 MMA issuer and TMEM
+// Q_i with L_i, D_i through a 2-slot ring, dO_i through one slot at d = 128;
+// three slots each at d = 64), warp 1 MMA issuer and TMEM
 // owner, warps 2-9 compute P^T and dS^T (one thread per key row, two warps per
 // TMEM lane quarter splitting the step's 128 query columns) and then move
 // their half of dQ from TMEM into the global accumulator; at the end warps
@@ -52,18 +56,26 @@ template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / kChunk;
   static constexpr int kTileBytes = kTileM * D * 2;        // one 128 x D tile
-  static constexpr int kStages = (D == 128) ? 2 : 3;       // Q/dO ring depth
+  // Q_i (with its L and D rows) is live from S^T(i), issued during the step
+  // before, to dK(i): two or three slots. dO_i is live from dP^T(i) to dV(i),
+  // which follow each other: d = 128 keeps one slot and spends the space on
+  // the dQ staging of the bulk reductions.
+  static constexpr int kQStages = (D == 128) ? 2 : 3;
+  static constexpr int kDoStages = (D == 128) ? 1 : 3;
+  static constexpr bool kBulkDq = (D == 128);
   static constexpr int kDsBytes = kTileN * kTileM * 2;     // dS^T, 128 x 128 16-bit
+  static constexpr int kDqStageBytes = 32 * 32 * 4;        // per compute warp: 32 rows x 32 fp32
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;                 // [stages]
-  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // [stages]
-  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
-  static constexpr int kOffRow = kOffDS + kDsBytes;                // [stages] x (L2 | D) x 128 f32
-  static constexpr int kOffBar = kOffRow + kStages * 1024;
-  // kv_full, qdo_full[S], qdo_empty[S], s_full, dp_full, p_full, ds_full,
-  // dv_done, dq_full, dq_empty, ds_empty, kd_done, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 10;
+  static constexpr int kOffQ = kOffV + kTileBytes;                 // [kQStages]
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;     // [kDoStages]
+  static constexpr int kOffDS = kOffDO + kDoStages * kTileBytes;
+  static constexpr int kOffDqS = kOffDS + kDsBytes;                // [8 warps] (d = 128)
+  static constexpr int kOffRow = kOffDqS + (kBulkDq ? 8 * kDqStageBytes : 0);  // [kQStages] x (L2 | D) x 128 f32
+  static constexpr int kOffBar = kOffRow + kQStages * 1024;
+  // kv_full, q_full[NQ], q_empty[NQ], do_full[ND], do_empty[ND], s_full,
+  // dp_full, p_full, ds_full, dv_done, dq_full, dq_empty, ds_empty, kd_done, drain
+  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDoStages + 10;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
 };
@@ -155,12 +167,14 @@ template <int D, bool kBf16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using Cfg = BwdCfg<D>;
-  constexpr int NS = Cfg::kStages;
+  constexpr int NQ = Cfg::kQStages;
+  constexpr int ND = Cfg::kDoStages;
   // d = 128: dQ is formed transposed, dQ^T = K_j^T dS^T (TMEM lanes = head
-  // dimension), so each warp's reduction into the accumulator covers one
-  // contiguous 128-byte row segment. For d = 64 that would be an M = 64 MMA,
-  // so there dQ = dS K_j (TMEM lanes = query rows) and each thread adds its
-  // row with 16-byte vector reductions.
+  // dimension); each compute warp stages its 32 head-dimension columns x 32
+  // query rows in shared memory (one 128-byte row per query) and one lane adds
+  // the box into the accumulator with a bulk tensor reduce. For d = 64 that
+  // would be an M = 64 MMA, so there dQ = dS K_j (TMEM lanes = query rows) and
+  // each thread adds its row with 16-byte vector reductions.
   constexpr bool kDqT = (D == 128);
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -173,9 +187,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const uint32_t bar0 = sbase + Cfg::kOffBar;
   const uint32_t kv_full = bar0;
-  auto qdo_full = [&](int s) { return bar0 + 8 * (1 + s); };
-  auto qdo_empty = [&](int s) { return bar0 + 8 * (1 + NS + s); };
-  const uint32_t s_full = bar0 + 8 * (1 + 2 * NS);
+  auto q_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto q_empty = [&](int s) { return bar0 + 8 * (1 + NQ + s); };
+  auto do_full = [&](int s) { return bar0 + 8 * (1 + 2 * NQ + s); };
+  auto do_empty = [&](int s) { return bar0 + 8 * (1 + 2 * NQ + ND + s); };
+  const uint32_t s_full = bar0 + 8 * (1 + 2 * NQ + 2 * ND);
   const uint32_t dp_full = s_full + 8;
   const uint32_t p_full = s_full + 16;
   const uint32_t ds_full = s_full + 24;
@@ -206,9 +222,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(qdo_full(s), 1);
-      mbar_init(qdo_empty(s), 1 + 8);   // MMA commit + one per compute warp
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 1 + 8);   // MMA commit + one per compute warp (L, D rows)
+    }
+    for (int s = 0; s < ND; ++s) {
+      mbar_init(do_full(s), 1);
+      mbar_init(do_empty(s), 1);      // MMA commit after dV
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -247,30 +267,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     j * kTileN, bkv);
       }
       Tracer tr(p.trace, 0);
-      int it = 0;
-      for (; it < n_iter; ++it) {
-        const int st = it % NS;
-        const uint32_t use = static_cast<uint32_t>(it / NS);
-        if (it >= NS && !mbar_wait(qdo_empty(st), (use - 1) & 1, abort_flag, p.status)) break;
-        tr(41);
+      int nq = 0, ndo = 0;   // Q and dO tiles issued
+      for (int it = 0; it < n_iter; ++it) {
         const int bh = bh_of(it), i = i_of(it);
-        const uint32_t fb = qdo_full(st);
-        mbar_arrive_expect_tx(fb, 2 * Cfg::kTileBytes + 1024);
-        for (int c = 0; c < Cfg::kChunks; ++c) {
-          tma_load_3d(sbase + Cfg::kOffQ + st * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_q, fb,
+        const int sq = it % NQ;
+        if (it >= NQ &&
+            !mbar_wait(q_empty(sq), static_cast<uint32_t>(it / NQ - 1) & 1, abort_flag, p.status))
+          break;
+        tr(41);
+        const uint32_t fq = q_full(sq);
+        mbar_arrive_expect_tx(fq, Cfg::kTileBytes + 1024);
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(sbase + Cfg::kOffQ + sq * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_q, fq,
                       c * kChunk, i * kTileM, bh);
-          tma_load_3d(sbase + Cfg::kOffDO + st * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_do,
-                      fb, c * kChunk, i * kTileM, bh);
-        }
         const size_t roff = static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM;
-        bulk_load(sbase + Cfg::kOffRow + st * 1024, p.lse2 + roff, 512, fb);
-        bulk_load(sbase + Cfg::kOffRow + st * 1024 + 512, p.delta + roff, 512, fb);
+        bulk_load(sbase + Cfg::kOffRow + sq * 1024, p.lse2 + roff, 512, fq);
+        bulk_load(sbase + Cfg::kOffRow + sq * 1024 + 512, p.delta + roff, 512, fq);
+        ++nq;
+        const int sd = it % ND;
+        if (it >= ND &&
+            !mbar_wait(do_empty(sd), static_cast<uint32_t>(it / ND - 1) & 1, abort_flag, p.status))
+          break;
+        const uint32_t fd = do_full(sd);
+        mbar_arrive_expect_tx(fd, Cfg::kTileBytes);
+        for (int c = 0; c < Cfg::kChunks; ++c)
+          tma_load_3d(sbase + Cfg::kOffDO + sd * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_do,
+                      fd, c * kChunk, i * kTileM, bh);
+        ++ndo;
         tr(40);
       }
       if (*abort_flag) {
         drain_wait(kv_full, 0, p.status);
-        for (int jj = max(0, it - NS); jj < it; ++jj)
-          drain_wait(qdo_full(jj % NS), static_cast<uint32_t>(jj / NS) & 1, p.status);
+        for (int jj = max(0, nq - NQ); jj < nq; ++jj)
+          drain_wait(q_full(jj % NQ), static_cast<uint32_t>(jj / NQ) & 1, p.status);
+        for (int jj = max(0, ndo - ND); jj < ndo; ++jj)
+          drain_wait(do_full(jj % ND), static_cast<uint32_t>(jj / ND) & 1, p.status);
       }
     }
   } else if (warp == 1) {
@@ -288,7 +319,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t k_s = sbase + Cfg::kOffK, v_s = sbase + Cfg::kOffV;
       const uint32_t ds_s = sbase + Cfg::kOffDS;
       auto q_s = [&](int st) { return sbase + Cfg::kOffQ + st * Cfg::kTileBytes; };
-      auto do_s = [&](int st) { return sbase + Cfg::kOffDO + st * Cfg::kTileBytes; };
+      auto do_s = [&](int sd) { return sbase + Cfg::kOffDO + sd * Cfg::kTileBytes; };
 
       auto issue_s = [&](int st) {   // S^T = K_j Q_i^T
 #pragma unroll
@@ -311,7 +342,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
       Tracer tr(p.trace, 1);
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.status) &&
-                mbar_wait(qdo_full(0), 0, abort_flag, p.status);
+                mbar_wait(q_full(0), 0, abort_flag, p.status) &&
+                mbar_wait(do_full(0), 0, abort_flag, p.status);
       tr(9);
       if (ok) {
         tc_fence_after();
@@ -319,8 +351,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_dp(0);
       }
       for (int n = 0; ok && n < n_iter; ++n) {
-        const int st = n % NS;
-        const int st1 = (n + 1) % NS;
+        const int st = n % NQ;
+        const int st1 = (n + 1) % NQ;
+        const int sd = n % ND;
+        const int sd1 = (n + 1) % ND;
         const bool more = n + 1 < n_iter;
         // dV += P^T dO_i  (P^T from TMEM, 16-bit packed: query columns 0-63 in
         // S^T's columns 0-31, columns 64-127 in S^T's columns 96-127)
@@ -330,9 +364,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kTileM / 16; ++ks)
           mma_ts(t_dv, t_s + ks * 8 + (ks >= 4 ? 64 : 0),
-                 make_sdesc(do_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
+                 make_sdesc(do_s(sd) + ks * 2048, kTileM * 128, 1024), idesc_kv,
                  (n > 0 || ks > 0) ? 1u : 0u);
         tc_commit(dv_done);
+        tc_commit(do_empty(sd));
         // dQ (into dP^T's columns: the compute warps have read dP^T(n))
         if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, p.status))) break;
         tr(3);
@@ -349,7 +384,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_commit(dq_full);
         // S^T for the next step, once dV(n) has consumed P^T(n)
         if (more) {
-          if (!(ok = mbar_wait(qdo_full(st1), static_cast<uint32_t>((n + 1) / NS) & 1,
+          if (!(ok = mbar_wait(q_full(st1), static_cast<uint32_t>((n + 1) / NQ) & 1,
                                abort_flag, p.status)))
             break;
           if (!(ok = mbar_wait(dv_done, n & 1, abort_flag, p.status))) break;
@@ -364,14 +399,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  make_sdesc(q_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
                  (n > 0 || ks > 0) ? 1u : 0u);
         tc_commit(ds_empty);
-        tc_commit(qdo_empty(st));
+        tc_commit(q_empty(st));
         tr(6);
         // dP^T for the next step, once dQ(n) has left TMEM
         if (more) {
           if (!(ok = mbar_wait(dq_empty, n & 1, abort_flag, p.status))) break;
+          if (!(ok = mbar_wait(do_full(sd1), static_cast<uint32_t>((n + 1) / ND) & 1, abort_flag,
+                               p.status)))
+            break;
           tr(7);
           tc_fence_after();
-          issue_dp(st1);
+          issue_dp(sd1);
         }
       }
       tc_commit(ok ? kd_done : drain);
@@ -397,14 +435,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* ds_row = smem + Cfg::kOffDS + half * (kTileN * 128) + r * 128;
     Tracer tr((warp == 2 && lane == 0) ? p.trace : nullptr, 2);
     bool ok = true;
+    // d = 128: this warp's dQ staging box (32 query rows x 32 fp32). Each
+    // step's 64 query rows go out as two boxes: the first right after the
+    // read-out, the second (held in registers meanwhile) after the next
+    // step's P^T, by when the first box has long been read; so the warps
+    // never wait on the reduce's progress inside the read-out.
+    const uint32_t dq_stage = sbase + Cfg::kOffDqS + (warp - 2) * Cfg::kDqStageBytes;
+    float* dq_stage_p = reinterpret_cast<float*>(smem + Cfg::kOffDqS + (warp - 2) * Cfg::kDqStageBytes);
+    uint32_t dq_pend[32];
+    int pend_y = -1, pend_bh = 0;
+    // stage 32 values per lane (lane = head-dimension column, conflict-free),
+    // hand them to the async proxy and let one lane issue the reduce-add
+    auto reduce_box = [&](const uint32_t* v, int y, int bh) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 32; ++q) dq_stage_p[q * 32 + lane] = __uint_as_float(v[q]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&p.tm_dq, dq_stage, quarter * 32, y, bh);
+        bulk_commit_group();
+      }
+    };
     for (int it = 0; it < n_iter; ++it) {
-      const int st = it % NS;
-      const uint32_t par = static_cast<uint32_t>(it / NS) & 1;
+      const int st = it % NQ;
+      const uint32_t par = static_cast<uint32_t>(it / NQ) & 1;
       const int i = i_of(it);
       const float* rowv = reinterpret_cast<const float*>(smem + Cfg::kOffRow + st * 1024);
       const float* l2s = rowv + c0;          // L * log2(e) per query column
       const float* dls = rowv + 128 + c0;    // D per query column
-      ok = __all_sync(0xffffffffu, mbar_wait(qdo_full(st), par, abort_flag, p.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(q_full(st), par, abort_flag, p.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, p.status));
       if (!ok) break;
       tr(20);
@@ -439,6 +500,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
       tr(21);
+      if constexpr (Cfg::kBulkDq) {
+        if (pend_y >= 0) reduce_box(dq_pend, pend_y, pend_bh);
+        pend_y = -1;
+        tr(34);
+      }
 
       if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (it - 1) & 1, abort_flag, p.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag, p.status));
@@ -470,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(ds_full);
-        mbar_arrive(qdo_empty(st));
+        mbar_arrive(q_empty(st));
       }
       tr(23);
 
@@ -496,7 +562,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tr(31);
       const int bh = bh_of(it);
       float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM) * D;
-      if constexpr (kDqT) {
+      if constexpr (Cfg::kBulkDq) {
+        reduce_box(acc, i * kTileM + c0, bh);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
+        pend_y = i * kTileM + c0 + 32;
+        pend_bh = bh;
+        (void)tile;
+      } else if constexpr (kDqT) {
         float* col = tile + static_cast<size_t>(c0) * D + r;
 #pragma unroll
         for (int q = 0; q < 64; ++q) atomicAdd(col + q * D, __uint_as_float(acc[q]));
@@ -508,6 +581,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                          __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
       }
       tr(32);
+    }
+    if constexpr (Cfg::kBulkDq) {
+      if (ok && pend_y >= 0) reduce_box(dq_pend, pend_y, pend_bh);
+      // the bulk reduces read this warp's staging box until they complete
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
     // ---- epilogue: warps 2-5 write dK = scale * accumulated dS^T Q, warps 6-9 dV ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
