@@ -63,7 +63,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int BH, int S, int d, bool bf16
 }
 
 // 3-D view [BH][S_pad][d] of the fp32 dQ accumulator for bulk reduce-adds;
-// box = 32 columns (128 bytes) x 32 rows x 1 head, no swizzle.
+// box = 32 columns (128 bytes) x 32 rows x 1 head, 128-byte swizzle.
 bool make_tmap_acc(CUtensorMap* m, float* base, int BH, int S_pad, int d) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -73,7 +73,7 @@ bool make_tmap_acc(CUtensorMap* m, float* base, int BH, int S_pad, int d) {
   cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -169,13 +169,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using Cfg = BwdCfg<D>;
   constexpr int NQ = Cfg::kQStages;
   constexpr int ND = Cfg::kDoStages;
-  // d = 128: dQ is formed transposed, dQ^T = K_j^T dS^T (TMEM lanes = head
-  // dimension); each compute warp stages its 32 head-dimension columns x 32
-  // query rows in shared memory (one 128-byte row per query) and one lane adds
-  // the box into the accumulator with a bulk tensor reduce. For d = 64 that
-  // would be an M = 64 MMA, so there dQ = dS K_j (TMEM lanes = query rows) and
-  // each thread adds its row with 16-byte vector reductions.
-  constexpr bool kDqT = (D == 128);
+  // dQ = dS K_j lands in TMEM with lanes = query rows, so each compute thread
+  // holds D/2 consecutive accumulator entries of one query row. d = 128: each
+  // warp stages them as boxes of 32 rows x 32 fp32 (128-byte rows, 128-byte
+  // swizzle: 16-byte stores, conflict-free) and one lane adds a box into the
+  // accumulator with a bulk tensor reduce. d = 64: each thread adds its row
+  // with 16-byte vector reductions.
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {   // the 128-byte swizzle needs 1024-byte aligned tiles
@@ -313,8 +312,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kTileM, kBf16, false, false);  // S^T, dP^T
       constexpr uint32_t idesc_kv = make_idesc(128, D, kBf16, false, true);       // dV, dK
-      constexpr uint32_t idesc_q = kDqT ? make_idesc(128, kTileM, kBf16, true, true)
-                                        : make_idesc(128, D, kBf16, true, true);  // dQ^T / dQ
+      constexpr uint32_t idesc_q = make_idesc(128, D, kBf16, true, true);         // dQ
       const uint32_t t_dk = tmem, t_dv = tmem + 128, t_s = tmem + 256, t_dp = tmem + 384;
       const uint32_t k_s = sbase + Cfg::kOffK, v_s = sbase + Cfg::kOffV;
       const uint32_t ds_s = sbase + Cfg::kOffDS;
@@ -373,14 +371,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tr(3);
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTileN / 16; ++ks) {
-          if constexpr (kDqT)   // dQ^T = K_j^T dS^T
-            mma_ss(t_dp, make_sdesc(k_s + ks * 2048, kTileN * 128, 1024),
-                   make_sdesc(ds_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
-          else                  // dQ = dS K_j
-            mma_ss(t_dp, make_sdesc(ds_s + ks * 2048, kTileN * 128, 1024),
-                   make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
-        }
+        for (int ks = 0; ks < kTileN / 16; ++ks)   // dQ = dS K_j, both operands MN-major
+          mma_ss(t_dp, make_sdesc(ds_s + ks * 2048, kTileN * 128, 1024),
+                 make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
         tc_commit(dq_full);
         // S^T for the next step, once dV(n) has consumed P^T(n)
         if (more) {
@@ -435,26 +428,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* ds_row = smem + Cfg::kOffDS + half * (kTileN * 128) + r * 128;
     Tracer tr((warp == 2 && lane == 0) ? p.trace : nullptr, 2);
     bool ok = true;
-    // d = 128: this warp's dQ staging box (32 query rows x 32 fp32). Each
-    // step's 64 query rows go out as two boxes: the first right after the
+    // d = 128: this warp's dQ staging box (its 32 query rows x 32 fp32).
+    // Each step's 64 columns go out as two boxes: the first right after the
     // read-out, the second (held in registers meanwhile) after the next
     // step's P^T, by when the first box has long been read; so the warps
     // never wait on the reduce's progress inside the read-out.
     const uint32_t dq_stage = sbase + Cfg::kOffDqS + (warp - 2) * Cfg::kDqStageBytes;
-    float* dq_stage_p = reinterpret_cast<float*>(smem + Cfg::kOffDqS + (warp - 2) * Cfg::kDqStageBytes);
+    // row `lane` with the swizzle's row term folded in: unit u is at row_sw ^ (u << 4)
+    const uint32_t row_sw = dq_stage + lane * 128 + ((lane & 7) << 4);
     uint32_t dq_pend[32];
-    int pend_y = -1, pend_bh = 0;
-    // stage 32 values per lane (lane = head-dimension column, conflict-free),
-    // hand them to the async proxy and let one lane issue the reduce-add
-    auto reduce_box = [&](const uint32_t* v, int y, int bh) {
+    int pend_x = -1, pend_y = 0, pend_bh = 0;
+    // stage this lane's 32 values as row `lane` of the box (16-byte unit u at
+    // u ^ (lane % 8): the map's 128-byte swizzle), hand the box to the async
+    // proxy and let one lane issue the reduce-add
+    auto reduce_box = [&](const uint32_t* v, int x, int y, int bh) {
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
 #pragma unroll
-      for (int q = 0; q < 32; ++q) dq_stage_p[q * 32 + lane] = __uint_as_float(v[q]);
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(row_sw ^ (u << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(&p.tm_dq, dq_stage, quarter * 32, y, bh);
+        tma_reduce_add_3d(&p.tm_dq, dq_stage, x, y, bh);
         bulk_commit_group();
       }
     };
@@ -501,8 +497,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(p_full);
       tr(21);
       if constexpr (Cfg::kBulkDq) {
-        if (pend_y >= 0) reduce_box(dq_pend, pend_y, pend_bh);
-        pend_y = -1;
+        if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
+        pend_x = -1;
         tr(34);
       }
 
@@ -540,21 +536,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tr(23);
 
-      // dQ(it): TMEM -> fp32 accumulator. d = 128: dQ^T (TMEM lanes = head
-      // dimension), the warp holds head-dimension entries of its quarter for
-      // its 64 query rows;
-      // d = 64: dQ (TMEM lanes = query rows), this thread adds 32 head-dimension
-      // entries (half `half`) of its query row with 16-byte reductions.
+      // dQ(it): TMEM -> fp32 accumulator. This thread holds head-dimension
+      // entries [half * D/2, (half + 1) * D/2) of query row r of the tile.
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
       if (!ok) break;
       tr(30);
       tc_fence_after();
-      constexpr int kCols = kDqT ? 64 : 32;
+      constexpr int kCols = D / 2;
       uint32_t acc[kCols];
 #pragma unroll
       for (int cc = 0; cc < kCols / 32; ++cc)
-        tmem_ld32(t_dp + (kDqT ? c0 : half * 32) + cc * 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
+        tmem_ld32(t_dp + half * kCols + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -563,16 +555,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int bh = bh_of(it);
       float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM) * D;
       if constexpr (Cfg::kBulkDq) {
-        reduce_box(acc, i * kTileM + c0, bh);
+        reduce_box(acc, half * 64, i * kTileM + quarter * 32, bh);
 #pragma unroll
         for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
-        pend_y = i * kTileM + c0 + 32;
+        pend_x = half * 64 + 32;
+        pend_y = i * kTileM + quarter * 32;
         pend_bh = bh;
         (void)tile;
-      } else if constexpr (kDqT) {
-        float* col = tile + static_cast<size_t>(c0) * D + r;
-#pragma unroll
-        for (int q = 0; q < 64; ++q) atomicAdd(col + q * D, __uint_as_float(acc[q]));
       } else {
         float4* row = reinterpret_cast<float4*>(tile + static_cast<size_t>(r) * D + half * 32);
 #pragma unroll
@@ -583,7 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tr(32);
     }
     if constexpr (Cfg::kBulkDq) {
-      if (ok && pend_y >= 0) reduce_box(dq_pend, pend_y, pend_bh);
+      if (ok && pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
       // the bulk reduces read this warp's staging box until they complete
       if (lane == 0) bulk_wait_all();
       __syncwarp();
