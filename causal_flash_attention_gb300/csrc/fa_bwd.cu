@@ -431,8 +431,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // d = 128: this warp's dQ staging box (its 32 query rows x 32 fp32).
     // Each step's 64 columns go out as two boxes: the first right after the
     // read-out, the second (held in registers meanwhile) after the next
-    // step's P^T, by when the first box has long been read; so the warps
-    // never wait on the reduce's progress inside the read-out.
+    // step's dS^T, while the warps would otherwise wait for dQ; by then the
+    // first box has long been read, and neither P^T -> dS^T nor the MMA
+    // chain waits on the reduce's progress.
     const uint32_t dq_stage = sbase + Cfg::kOffDqS + (warp - 2) * Cfg::kDqStageBytes;
     // row `lane` with the swizzle's row term folded in: unit u is at row_sw ^ (u << 4)
     const uint32_t row_sw = dq_stage + lane * 128 + ((lane & 7) << 4);
@@ -496,11 +497,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
       tr(21);
-      if constexpr (Cfg::kBulkDq) {
-        if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
-        pend_x = -1;
-        tr(34);
-      }
 
       if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (it - 1) & 1, abort_flag, p.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag, p.status));
@@ -535,6 +531,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(q_empty(st));
       }
       tr(23);
+      if constexpr (Cfg::kBulkDq) {
+        if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
+        pend_x = -1;
+        tr(34);
+      }
 
       // dQ(it): TMEM -> fp32 accumulator. This thread holds head-dimension
       // entries [half * D/2, (half + 1) * D/2) of query row r of the tile.
