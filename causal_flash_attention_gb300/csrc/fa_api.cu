@@ -298,7 +298,7 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
   std::memset(&p, 0, sizeof(p));
   if (!make_tmap(&p.tm_q, q, BH, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
       !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16) ||
-      (d == 128 && !make_tmap_acc(&p.tm_dq, pre.dq_acc, BH, Sq_pad, d)))
+      !make_tmap_acc(&p.tm_dq, pre.dq_acc, BH, Sq_pad, d))
     return FA_ERR_TMA;
   p.delta = pre.delta;
   p.lse2 = pre.lse2;

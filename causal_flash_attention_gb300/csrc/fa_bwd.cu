@@ -23,10 +23,9 @@
 //                    dV  += P^T dO_i           (P^T from TMEM)
 //                    dK  += dS^T Q_i
 //                    dQ   = dS K_j             -> TMEM, then added into the fp32
-//                                                 dQ accumulator (d = 128: bulk
-//                                                 tensor reduce-adds of boxes staged
-//                                                 in shared memory; d = 64: 16-byte
-//                                                 vector atomics)
+//                                                 dQ accumulator by bulk tensor
+//                                                 reduce-adds of boxes staged in
+//                                                 shared memory
 //   3. dq_convert: dq = scale * accumulator, rounded to the input type.
 //
 // Warp roles of bwd_main (320 threads): warp 0 TMA producer (K_j, V_j once;
@@ -62,7 +61,6 @@ struct BwdCfg {
   // the dQ staging of the bulk reductions.
   static constexpr int kQStages = (D == 128) ? 2 : 3;
   static constexpr int kDoStages = (D == 128) ? 1 : 3;
-  static constexpr bool kBulkDq = (D == 128);
   static constexpr int kDsBytes = kTileN * kTileM * 2;     // dS^T, 128 x 128 16-bit
   static constexpr int kDqStageBytes = 32 * 32 * 4;        // per compute warp: 32 rows x 32 fp32
   static constexpr int kOffK = 0;
@@ -71,7 +69,7 @@ struct BwdCfg {
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;     // [kDoStages]
   static constexpr int kOffDS = kOffDO + kDoStages * kTileBytes;
   static constexpr int kOffDqS = kOffDS + kDsBytes;                // [8 warps] (d = 128)
-  static constexpr int kOffRow = kOffDqS + (kBulkDq ? 8 * kDqStageBytes : 0);  // [kQStages] x (L2 | D) x 128 f32
+  static constexpr int kOffRow = kOffDqS + 8 * kDqStageBytes;     // [kQStages] x (L2 | D) x 128 f32
   static constexpr int kOffBar = kOffRow + kQStages * 1024;
   // kv_full, q_full[NQ], q_empty[NQ], do_full[ND], do_empty[ND], s_full,
   // dp_full, p_full, ds_full, dv_done, dq_full, dq_empty, ds_empty, kd_done, drain
@@ -170,11 +168,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int NQ = Cfg::kQStages;
   constexpr int ND = Cfg::kDoStages;
   // dQ = dS K_j lands in TMEM with lanes = query rows, so each compute thread
-  // holds D/2 consecutive accumulator entries of one query row. d = 128: each
-  // warp stages them as boxes of 32 rows x 32 fp32 (128-byte rows, 128-byte
+  // holds D/2 consecutive accumulator entries of one query row. Each warp
+  // stages them as boxes of 32 rows x 32 fp32 (128-byte rows, 128-byte
   // swizzle: 16-byte stores, conflict-free) and one lane adds a box into the
-  // accumulator with a bulk tensor reduce. d = 64: each thread adds its row
-  // with 16-byte vector reductions.
+  // accumulator with a bulk tensor reduce.
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {   // the 128-byte swizzle needs 1024-byte aligned tiles
@@ -428,8 +425,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* ds_row = smem + Cfg::kOffDS + half * (kTileN * 128) + r * 128;
     Tracer tr((warp == 2 && lane == 0) ? p.trace : nullptr, 2);
     bool ok = true;
-    // d = 128: this warp's dQ staging box (its 32 query rows x 32 fp32).
-    // Each step's 64 columns go out as two boxes: the first right after the
+    // This warp's dQ staging box (its 32 query rows x 32 fp32). d = 64: the
+    // step's 32 columns are one box, staged right after the read-out.
+    // d = 128: the step's 64 columns go out as two boxes: the first right after the
     // read-out, the second (held in registers meanwhile) after the next
     // step's dS^T, while the warps would otherwise wait for dQ; by then the
     // first box has long been read, and neither P^T -> dS^T nor the MMA
@@ -531,7 +529,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(q_empty(st));
       }
       tr(23);
-      if constexpr (Cfg::kBulkDq) {
+      if constexpr (D == 128) {
         if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
         pend_x = -1;
         tr(34);
@@ -554,30 +552,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(dq_empty);
       tr(31);
       const int bh = bh_of(it);
-      float* tile = p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + static_cast<size_t>(i) * kTileM) * D;
-      if constexpr (Cfg::kBulkDq) {
+      if constexpr (D == 128) {
         reduce_box(acc, half * 64, i * kTileM + quarter * 32, bh);
 #pragma unroll
         for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
         pend_x = half * 64 + 32;
         pend_y = i * kTileM + quarter * 32;
         pend_bh = bh;
-        (void)tile;
-      } else {
-        float4* row = reinterpret_cast<float4*>(tile + static_cast<size_t>(r) * D + half * 32);
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          atomicAdd(row + v, make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
-                                         __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3])));
+      } else {   // d = 64: the step's 32 columns are one box
+        reduce_box(acc, half * 32, i * kTileM + quarter * 32, bh);
       }
       tr(32);
     }
-    if constexpr (Cfg::kBulkDq) {
-      if (ok && pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
-      // the bulk reduces read this warp's staging box until they complete
-      if (lane == 0) bulk_wait_all();
-      __syncwarp();
-    }
+    if (ok && pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
+    // the bulk reduces read this warp's staging box until they complete
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     // ---- epilogue: warps 2-5 write dK = scale * accumulated dS^T Q, warps 6-9 dV ----
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
     if (ok) {

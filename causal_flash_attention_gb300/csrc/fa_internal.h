@@ -50,7 +50,7 @@ struct BwdParams {
   CUtensorMap tm_k;   // [B*Hkv][Skv][d]
   CUtensorMap tm_v;   // [B*Hkv][Skv][d]
   CUtensorMap tm_do;  // [B*Hq][Sq][d]
-  CUtensorMap tm_dq;  // dq_acc as fp32 [B*Hq][Sq_pad][d], box (32, 32, 1), 128B swizzle (d = 128)
+  CUtensorMap tm_dq;  // dq_acc as fp32 [B*Hq][Sq_pad][d], box (32, 32, 1), 128B swizzle
   const float* delta; // [B*Hq][Sq_pad]
   const float* lse2;  // [B*Hq][Sq_pad]
   float* dq_acc;      // [B*Hq][Sq_pad][d]
