@@ -323,6 +323,8 @@ def run_gpu(args, w, rank, world, local_rank):
         total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
         fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
         bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        fwd_med = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+        bwd_med = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
 
         # End to end through the public API with host buffers: every step
         # copies its inputs from pinned host memory, runs fa_fwd + fa_bwd and
@@ -398,8 +400,10 @@ def run_gpu(args, w, rank, world, local_rank):
     if status:
         raise RuntimeError(f"device status {status} in the timed region")
 
-    total_ms, fwd_ms, bwd_ms, e2e_ms = max_over_ranks([total_ms, fwd_ms, bwd_ms, e2e_ms], dist, dev)
+    total_ms, fwd_ms, bwd_ms, e2e_ms, fwd_med, bwd_med = max_over_ranks(
+        [total_ms, fwd_ms, bwd_ms, e2e_ms, fwd_med, bwd_med], dist, dev)
     return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms,
+                fwd_med_ms=fwd_med, bwd_med_ms=bwd_med,
                 h2d=h2d, d2h=d2h, clocks=clocks.summary(), dist=dist,
                 launches_per_fwd=(2 if dec_ws_bytes else 1))
 
@@ -408,7 +412,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="long_8k", choices=sorted(fa_inputs.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -498,6 +502,11 @@ def main():
                         "step_vs_sustained": 100 * value / world / peaks["bf16_tflops_sustained"]},
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
+        "per_call_median": {"fwd_ms": r["fwd_med_ms"],
+                            "bwd_ms": r["bwd_med_ms"] if w.backward else None,
+                            "fwd_tflops": flops(w, True, False) / (r["fwd_med_ms"] * 1e-3) / 1e12,
+                            "bwd_tflops": (flops(w, False, True) / (r["bwd_med_ms"] * 1e-3) / 1e12
+                                           if w.backward else None)},
         "roofline": {
             "kernel": "fa_bwd_kernel (timed as the fa_bwd call: D pre-pass + main kernel + dQ convert)",
             "bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
