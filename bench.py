@@ -197,6 +197,26 @@ def cpu_threads():
         return os.cpu_count() or 1, "cores available (BLAS default)"
 
 
+def cpu_model():
+    """The host CPU's model name as lscpu or /proc/cpuinfo report it (None if neither does)."""
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def oracle_inputs(w, heads):
     """float64 copies of batch 0, query heads [0, heads) and their key/value heads."""
     import torch
@@ -469,7 +489,8 @@ def main():
                 "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
-                                 "cores_source": how, "kind": "oracle", "sample": sample},
+                                 "cores_source": how, "cpu_model": cpu_model(), "kind": "oracle",
+                                 "sample": sample},
                 "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0},
                 "gpu_launches": 0}
@@ -561,7 +582,7 @@ def main():
             total_f += fl
         line["cpu_baseline"] = {
             "value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": cores,
-            "cores_source": how, "kind": "oracle",
+            "cores_source": how, "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"fp64 dense forward{' + softmax-Jacobian backward' if w.backward else ''} "
                       f"of the leading block (query rows 0..{block[0] - 1}, keys 0..{block[1] - 1}) "
                       f"of query heads 0 and 1 of {w.name} (all of each head when the block "
