@@ -434,10 +434,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 // ------------------------------------------------------------------ merge --
-// One warp per output row (b, hq, s). The lanes first read the ranges'
-// lse2 in parallel (lane i: ranges i, i + 32, ...) and reduce M and the
-// weights with shuffles; then each lane combines d / 32 columns of the
-// ranges' partial rows, four ranges' loads in flight at a time.
+// One warp per output row (b, hq, s); each lane owns d / 32 columns. The
+// merge is latency-bound (a few KB per row), so the loads are batched: the
+// first batch of up to kMergeBatch ranges' partial rows and their lse2 values
+// is issued before the maximum over all ranges' lse2 is reduced (lane i reads
+// ranges i, i + 32, ...), and every lane forms the same weights
+// 2^(lse2 - M) from broadcast reads, so the row sum needs no reduction.
+constexpr int kMergeBatch = 16;
+
+template <int PER>
+struct alignas(4 * PER) MergeVec { float x[PER]; };
+
 template <typename T, int PER>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeMergeParams p) {
   // Launched as a programmatic dependent of the split kernel: wait until that
@@ -452,30 +459,48 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeMergePara
   const int bkv = b * p.Hkv + hq / p.G;
   const int r = (hq % p.G) * p.Sq + s;
   const size_t base = static_cast<size_t>(bkv) * p.n_splits;
+  const int n = p.n_splits;
+  using V = MergeVec<PER>;
+  auto part = [&](int sp) {
+    return reinterpret_cast<const V*>(p.part_out + ((base + sp) * p.R + r) * p.d)[lane];
+  };
+  auto lse2_of = [&](int sp) { return p.part_lse2[(base + sp) * p.R + r]; };
+
+  V v[kMergeBatch];
+  float lv[kMergeBatch];
+#pragma unroll
+  for (int k = 0; k < kMergeBatch; ++k)
+    if (k < n) {
+      v[k] = part(k);
+      lv[k] = lse2_of(k);
+    }
   float M = -INFINITY;
-  for (int sp = lane; sp < p.n_splits; sp += 32) M = fmaxf(M, p.part_lse2[(base + sp) * p.R + r]);
+  for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, lse2_of(sp));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
-  for (int sp0 = 0; sp0 < p.n_splits; sp0 += 32) {
-    const int sp = sp0 + lane;
-    const float wl = (sp < p.n_splits && M != -INFINITY) ? ex2(p.part_lse2[(base + sp) * p.R + r] - M)
-                                                          : 0.f;
-    L += wl;
-    const int cnt = min(32, p.n_splits - sp0);
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, wl, k);
-      const float* src = p.part_out + ((base + sp0 + k) * p.R + r) * p.d + lane * PER;
+  for (int sp0 = 0; sp0 < n; sp0 += kMergeBatch) {
+    if (sp0 > 0) {
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = fmaf(wk, src[e], acc[e]);
+      for (int k = 0; k < kMergeBatch; ++k)
+        if (sp0 + k < n) {
+          v[k] = part(sp0 + k);
+          lv[k] = lse2_of(sp0 + k);
+        }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int k = 0; k < kMergeBatch; ++k)
+      if (sp0 + k < n) {
+        const float w = M != -INFINITY ? ex2(lv[k] - M) : 0.f;   // an empty range has lse2 = -inf
+        L += w;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[k].x[e], acc[e]);
+      }
+  }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   T* dst = static_cast<T*>(p.out) + row * p.d + lane * PER;
 #pragma unroll
