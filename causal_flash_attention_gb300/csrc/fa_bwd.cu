@@ -98,42 +98,50 @@ template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ------------------------------------------------------------------ pre --
-// One warp per (head row, query row) in [0, Sq_pad): D = <dO, O> in fp32,
-// L*log2(e), and a zeroed dQ accumulator row.
+// Rows [0, BH * Sq_pad): D = <dO, O> in fp32, L * log2(e), and a zeroed dQ
+// accumulator row. Bandwidth-bound, so every access is a 16-byte vector and
+// the grid is one wave of warps striding over the rows: a row is U = d *
+// sizeof(T) / 16 lanes (4 to 32), a warp takes 32 / U rows per pass.
+template <typename T>
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b) {
+  const T* x = reinterpret_cast<const T*>(&a);
+  const T* y = reinterpret_cast<const T*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < static_cast<int>(16 / sizeof(T)); ++e) s = fmaf(to_f(x[e]), to_f(y[e]), s);
+  return s;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // bh * Sq_pad + i
-  if (row >= static_cast<long long>(p.BH) * p.Sq_pad) return;
-  const int bh = static_cast<int>(row / p.Sq_pad), i = static_cast<int>(row % p.Sq_pad);
-  float dsum = 0.f;
-  if (i < p.Sq) {
-    // d / 32 (2 or 4) consecutive elements per lane, one vector load each
-    const size_t off = (static_cast<size_t>(bh) * p.Sq + i) * p.d;
-    const T* o = static_cast<const T*>(p.out) + off;
-    const T* g = static_cast<const T*>(p.dout) + off;
-    const int per = p.d / 32;
-    if (per == 4) {
-      struct alignas(4 * sizeof(T)) V4 { T x[4]; };
-      const V4 ov = reinterpret_cast<const V4*>(o)[lane], gv = reinterpret_cast<const V4*>(g)[lane];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) dsum = fmaf(to_f(ov.x[e]), to_f(gv.x[e]), dsum);
-    } else {
-      struct alignas(2 * sizeof(T)) V2 { T x[2]; };
-      const V2 ov = reinterpret_cast<const V2*>(o)[lane], gv = reinterpret_cast<const V2*>(g)[lane];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) dsum = fmaf(to_f(ov.x[e]), to_f(gv.x[e]), dsum);
+  const int lane = threadIdx.x & 31;
+  const int U = p.d * static_cast<int>(sizeof(T)) / 16;   // power of two, divides 32
+  const int rpw = 32 / U;
+  const int sub = lane / U, u = lane % U;
+  const long long total = static_cast<long long>(p.BH) * p.Sq_pad;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long row0 = warp0 * rpw; row0 < total; row0 += nwarps * rpw) {   // warp-uniform
+    const long long row = row0 + sub;                                       // bh * Sq_pad + i
+    const bool live = row < total;
+    const int bh = live ? static_cast<int>(row / p.Sq_pad) : 0;
+    const int i = live ? static_cast<int>(row % p.Sq_pad) : 0;
+    float dsum = 0.f;
+    if (live && i < p.Sq) {
+      const size_t off = (static_cast<size_t>(bh) * p.Sq + i) * p.d * sizeof(T);
+      const uint4 ov = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.out) + off)[u];
+      const uint4 gv = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.dout) + off)[u];
+      dsum = dot16<T>(ov, gv);
     }
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
-  if (lane == 0) {
-    p.delta[row] = (i < p.Sq) ? dsum : 0.f;
-    p.lse2[row] = (i < p.Sq) ? p.lse[static_cast<size_t>(bh) * p.Sq + i] * kLog2eF : INFINITY;
-  }
-  if (p.dq_acc) {
-    float4* acc = reinterpret_cast<float4*>(p.dq_acc + static_cast<size_t>(row) * p.d);
-    for (int e = lane; e < p.d / 4; e += 32) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sft = U / 2; sft > 0; sft >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, sft);
+    if (live && u == 0) {
+      p.delta[row] = (i < p.Sq) ? dsum : 0.f;
+      p.lse2[row] = (i < p.Sq) ? p.lse[static_cast<size_t>(bh) * p.Sq + i] * kLog2eF : INFINITY;
+    }
+    if (p.dq_acc && live) {
+      float4* acc = reinterpret_cast<float4*>(p.dq_acc + static_cast<size_t>(row) * p.d);
+      for (int e = u; e < p.d / 4; e += U) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -617,8 +625,12 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
+  // one wave of 8-warp blocks (8 per SM), fewer when the rows run out
   const long long rows = static_cast<long long>(p.BH) * p.Sq_pad;
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  const int esize = p.dtype == 0 ? 4 : 2;
+  const long long rows_per_block = 8LL * (32 / (p.d * esize / 16));
+  const unsigned grid =
+      static_cast<unsigned>(std::min<long long>((rows + rows_per_block - 1) / rows_per_block, 152LL * 8));
   if (p.dtype == 0) bwd_pre_kernel<float><<<grid, 256, 0, stream>>>(p);
   else if (p.dtype == 1) bwd_pre_kernel<__half><<<grid, 256, 0, stream>>>(p);
   else bwd_pre_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
