@@ -363,6 +363,7 @@ def run_gpu(args, w, rank, world, local_rank):
         h2d = sum(x.numel() * x.element_size() for x in ins_h)
         d2h = sum(x.numel() * x.element_size() for x in outs_h)
         K2 = 0 if args.no_e2e else max(3, K // 4)
+        link = None
         if K2:
             sets = []
             for sidx in range(2):
@@ -414,6 +415,20 @@ def run_gpu(args, w, rank, world, local_rank):
             e1.record(s_d2h)
             barrier()
             e2e_ms = e0.elapsed_time(e1) / K2
+
+            # the host link alone: one step's input copies, then its result
+            # copies, each timed by itself on its copy stream
+            def time_copies(cs, pairs):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(cs)
+                with torch.cuda.stream(cs):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+                b.record(cs)
+                torch.cuda.synchronize(dev)
+                return a.elapsed_time(b)
+            link = {"h2d_gbs": h2d / (time_copies(s_h2d, zip(sets[0][0], ins_h)) * 1e-3) / 1e9,
+                    "d2h_gbs": d2h / (time_copies(s_d2h, zip(outs_h, sets[0][1])) * 1e-3) / 1e9}
         else:
             e2e_ms = float("nan")
     status = fa.fa_last_device_status(stream)
@@ -424,7 +439,7 @@ def run_gpu(args, w, rank, world, local_rank):
         [total_ms, fwd_ms, bwd_ms, e2e_ms, fwd_med, bwd_med], dist, dev)
     return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms,
                 fwd_med_ms=fwd_med, bwd_med_ms=bwd_med,
-                h2d=h2d, d2h=d2h, clocks=clocks.summary(), dist=dist,
+                h2d=h2d, d2h=d2h, link=link, clocks=clocks.summary(), dist=dist,
                 launches_per_fwd=(2 if dec_ws_bytes else 1))
 
 
@@ -551,6 +566,7 @@ def main():
         },
         "e2e": {"value": e2e_tf, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
+                "host_link_gbs": r["link"],
                 "pipelining": "2 device buffer sets; H2D of step k and D2H of step k-1 on copy "
                               "streams overlap step k's kernels"},
         "gpu_launches": (r["launches_per_fwd"] + (3 if w.backward else 0)) * K,
