@@ -490,11 +490,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 64; ++e) raw[e] = (e < thr) ? __float_as_uint(-INFINITY) : raw[e];
         }
+        const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(raw[e]), c, -l2s[e]));
-          const float p1 = ex2(fmaf(__uint_as_float(raw[e + 1]), c, -l2s[e + 1]));
-          ppk[e / 2] = pack2<kBf16>(p0, p1);
+          const float2 l2 = *reinterpret_cast<const float2*>(l2s + e);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), c2,
+                           f2_pack(-l2.x, -l2.y)), x0, x1);
+          ppk[e / 2] = pack2<kBf16>(ex2(x0), ex2(x1));
         }
         tmem_st32(t_s + half * 96, ppk);
       }
@@ -518,8 +521,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           const float2 pp = unpack2<kBf16>(ppk[e / 2]);
-          const float d0 = pp.x * (__uint_as_float(raw[e]) - dls[e]);
-          const float d1 = pp.y * (__uint_as_float(raw[e + 1]) - dls[e + 1]);
+          const float2 dd = *reinterpret_cast<const float2*>(dls + e);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(pp.x, pp.y),
+                           f2_sub(f2_pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])),
+                                  f2_pack(dd.x, dd.y))), d0, d1);
           w[e / 2] = pack2<kBf16>(d0, d1);
         }
         // this warp's 64 query columns = one 128-byte row of chunk `half`;
