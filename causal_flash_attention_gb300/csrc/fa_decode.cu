@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         else mbar_arrive_expect_tx(v_full(st), Cfg::kTileBytes);
       }
       if (__shfl_sync(0xffffffffu, stop, 0)) {
-        ++j;   // this round's K load is in flight
+        ++j;   // this iteration's K load is in flight
         break;
       }
       load_part(&p.tm_v, sbase + Cfg::kOffV + st * Cfg::kTileBytes, v_full(st), tile, pb);

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(sbase + Cfg::kOffK + st * Cfg::kTileBytes + c * (kTileN * 128), &p.tm_k,
                       bars.kf(st), c * kChunk, j * kTileN, bkv);
         if (j >= NS && !mbar_wait(bars.ve(st), (use - 1) & 1, abort_flag, p.status)) {
-          ++j;   // the K load of this round is in flight
+          ++j;   // the K load of this iteration is in flight
           break;
         }
         mbar_arrive_expect_tx(bars.vf(st), Cfg::kTileBytes);
