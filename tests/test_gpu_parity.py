@@ -96,6 +96,9 @@ EDGE = [
     (1, 2, 2, 128, 64, "fp16"), (1, 8, 1, 129, 128, "bf16"), (2, 4, 4, 200, 64, "bf16"),
     (1, 2, 1, 255, 128, "fp16"), (1, 1, 1, 256, 64, "bf16"), (1, 2, 2, 257, 128, "bf16"),
     (1, 4, 1, 383, 64, "bf16"), (1, 2, 2, 640, 128, "bf16"),
+    # 16 query heads per key/value head: a backward CTA walks 16 heads' query
+    # tiles (and their dQ boxes) in one loop; ragged last tile
+    (1, 16, 1, 300, 128, "bf16"), (2, 16, 1, 200, 64, "fp16"),
     (1, 2, 1, 65, 64, "fp32"), (1, 2, 2, 130, 128, "fp32"), (1, 1, 1, 1, 64, "fp32"),
 ]
 
