@@ -84,6 +84,18 @@ def bwd_algorithmic_bytes(w):
     return 4 * q + 4 * kv + w.B * w.Hq * w.S * 4
 
 
+def hbm_side(nbytes, nflops, ms, peak_tflops, hbm_gbs):
+    """A call against the HBM roof: its algorithmic bytes over its time, its
+    arithmetic intensity and the ridge point between the tensor and HBM roofs
+    (None without a time or bytes)."""
+    if not ms or not nbytes:
+        return None
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"achieved_gbs": gbs, "peak_gbs": hbm_gbs, "frac": gbs / hbm_gbs,
+            "intensity_flop_per_byte": nflops / nbytes,
+            "ridge_flop_per_byte": peak_tflops * 1e12 / (hbm_gbs * 1e9)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -528,16 +540,6 @@ def main():
     e2e_tf = job_tflops(step_flops, world, r["e2e_ms"]) if r["e2e_ms"] == r["e2e_ms"] else None
     peak = peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"]
-
-    def hbm_side(nbytes, nflops, ms):
-        """The same call against the HBM roof: algorithmic bytes per call over its
-        time, the call's arithmetic intensity and the ridge point between the roofs."""
-        if not ms or not nbytes:
-            return None
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm,
-                "intensity_flop_per_byte": nflops / nbytes,
-                "ridge_flop_per_byte": peak * 1e12 / (hbm * 1e9)}
     traffic = recorded_traffic("fa_bwd_kernel", w.name)
     if args.heads:
         traffic = None
@@ -564,15 +566,16 @@ def main():
             "traffic_unit": "bytes per launch (dram read + write)",
             "algorithmic_bytes": bwd_algorithmic_bytes(w),
             "peak_source": f"{peak_src} bf16_tflops (burst)",
-            "hbm_side": hbm_side(bwd_algorithmic_bytes(w), flops(w, False, True), r["bwd_ms"])
-                        if w.backward else None,
+            "hbm_side": hbm_side(bwd_algorithmic_bytes(w), flops(w, False, True), r["bwd_ms"],
+                                 peak, hbm) if w.backward else None,
         },
         "roofline_fwd": {
             "kernel": "fa_fwd_kernel (one launch per fa_fwd call)", "bound": "tensor",
             "achieved": fwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
             "traffic": None if args.heads else recorded_traffic("fa_fwd_kernel", w.name),
             "algorithmic_bytes": fwd_algorithmic_bytes(w),
-            "hbm_side": hbm_side(fwd_algorithmic_bytes(w), flops(w, True, False), r["fwd_ms"]),
+            "hbm_side": hbm_side(fwd_algorithmic_bytes(w), flops(w, True, False), r["fwd_ms"],
+                                 peak, hbm),
         },
         "exp_ceiling": {
             "exps_per_step": int(w.B * w.Hq * visible_pairs(w.S, w.kv_len, w.causal)),
