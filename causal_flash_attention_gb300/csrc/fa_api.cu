@@ -2,6 +2,7 @@
 // TMA descriptor construction and kernel launches. No device memory is
 // allocated here; the only device-resident state is the status word below.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -38,9 +39,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Device address of g_status on the current device, looked up once per
+// device (the lookup is a runtime call worth microseconds of host time).
+constexpr int kMaxDevices = 128;
+std::atomic<int*> g_status_ptr[kMaxDevices];
+
 int* status_ptr() {
-  int* p = nullptr;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
   if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status) != cudaSuccess) return nullptr;
+  g_status_ptr[dev].store(p, std::memory_order_release);
   return p;
 }
 
@@ -265,44 +275,56 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
   const int Sq_pad = static_cast<int>(round_up(Sq, kTileM));
   const int kv_offset = causal ? Skv - Sq : 0;
 
+  float* delta = reinterpret_cast<float*>(wsb + ws.delta);
+  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  float* dq_acc = dtype == FA_F32 ? nullptr : reinterpret_cast<float*>(wsb + ws.dq_acc);
+  int* status = status_ptr();
+  if (!status) return FA_ERR_CUDA;
+
+  // Everything that can fail on the host (descriptor encoding, the status
+  // lookup) happens before the first kernel is enqueued.
+  const bool bf16 = dtype == FA_BF16;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (dtype != FA_F32 &&
+      (!make_tmap(&p.tm_q, q, BH, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
+       !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) ||
+       !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16) ||
+       !make_tmap_acc(&p.tm_dq, dq_acc, BH, Sq_pad, d)))
+    return FA_ERR_TMA;
+
   BwdPreParams pre;
   pre.out = out;
   pre.dout = dout;
   pre.lse = lse;
-  pre.delta = reinterpret_cast<float*>(wsb + ws.delta);
-  pre.lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
-  pre.dq_acc = dtype == FA_F32 ? nullptr : reinterpret_cast<float*>(wsb + ws.dq_acc);
+  pre.delta = delta;
+  pre.lse2 = lse2;
+  pre.dq_acc = dq_acc;
   pre.BH = BH; pre.Sq = Sq; pre.Sq_pad = Sq_pad; pre.d = d;
   pre.dtype = dtype;
   if (launch_bwd_pre(pre, st) != cudaSuccess) return FA_ERR_CUDA;
 
   if (dtype == FA_F32) {
-    SimtParams p{};
-    p.q = static_cast<const float*>(q);
-    p.k = static_cast<const float*>(k);
-    p.v = static_cast<const float*>(v);
-    p.dout = static_cast<const float*>(dout);
-    p.lse = lse;
-    p.delta = pre.delta;
-    p.dq = static_cast<float*>(dq);
-    p.dk = static_cast<float*>(dk);
-    p.dv = static_cast<float*>(dv);
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.kv_offset = kv_offset; p.d = d;
-    p.causal = causal != 0;
-    p.scale = scale;
-    return launch_bwd_simt(p, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    SimtParams sp{};
+    sp.q = static_cast<const float*>(q);
+    sp.k = static_cast<const float*>(k);
+    sp.v = static_cast<const float*>(v);
+    sp.dout = static_cast<const float*>(dout);
+    sp.lse = lse;
+    sp.delta = delta;
+    sp.dq = static_cast<float*>(dq);
+    sp.dk = static_cast<float*>(dk);
+    sp.dv = static_cast<float*>(dv);
+    sp.B = B; sp.Hq = Hq; sp.Hkv = Hkv; sp.Sq = Sq; sp.Skv = Skv; sp.kv_offset = kv_offset;
+    sp.d = d;
+    sp.causal = causal != 0;
+    sp.scale = scale;
+    return launch_bwd_simt(sp, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 
-  const bool bf16 = dtype == FA_BF16;
-  BwdParams p;
-  std::memset(&p, 0, sizeof(p));
-  if (!make_tmap(&p.tm_q, q, BH, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
-      !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) || !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16) ||
-      !make_tmap_acc(&p.tm_dq, pre.dq_acc, BH, Sq_pad, d))
-    return FA_ERR_TMA;
-  p.delta = pre.delta;
-  p.lse2 = pre.lse2;
-  p.dq_acc = pre.dq_acc;
+  p.delta = delta;
+  p.lse2 = lse2;
+  p.dq_acc = dq_acc;
   p.dk = dk;
   p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.Sq_pad = Sq_pad;
@@ -313,12 +335,11 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
   p.n_kv_tiles = (Skv + kTileN - 1) / kTileN;
   p.n_q_tiles = (Sq + kTileM - 1) / kTileM;
   p.trace = FA_TRACE_PTR;
-  p.status = status_ptr();
-  if (!p.status) return FA_ERR_CUDA;
+  p.status = status;
   if (launch_bwd_tc(p, d, bf16, st) != cudaSuccess) return FA_ERR_CUDA;
 
   DqConvertParams cv;
-  cv.dq_acc = pre.dq_acc;
+  cv.dq_acc = dq_acc;
   cv.dq = dq;
   cv.BH = BH; cv.Sq = Sq; cv.Sq_pad = Sq_pad; cv.d = d;
   cv.scale = scale;

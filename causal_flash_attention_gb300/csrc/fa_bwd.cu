@@ -324,22 +324,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto q_s = [&](int st) { return sbase + Cfg::kOffQ + st * Cfg::kTileBytes; };
       auto do_s = [&](int sd) { return sbase + Cfg::kOffDO + sd * Cfg::kTileBytes; };
 
-      auto issue_s = [&](int st) {   // S^T = K_j Q_i^T
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
-          mma_ss(t_s, make_sdesc(k_s + off, 16, 1024), make_sdesc(q_s(st) + off, 16, 1024),
-                 idesc_s, ks > 0);
-        }
+      // Every operand descriptor is formed once; each product is issued from
+      // one asm block with the K-step offsets as immediates (the issuing
+      // thread would otherwise spend longer forming descriptors than the
+      // tensor core spends on a step).
+      const uint64_t k_desc = make_sdesc(k_s, 16, 1024);              // K_j, K-major (S^T)
+      const uint64_t k_desc_mn = make_sdesc(k_s, kTileN * 128, 1024); // K_j, MN-major (dQ)
+      const uint64_t v_desc = make_sdesc(v_s, 16, 1024);              // V_j, K-major (dP^T)
+      const uint64_t ds_desc = make_sdesc(ds_s, 16, 1024);            // dS^T, K-major (dK)
+      const uint64_t ds_desc_mn = make_sdesc(ds_s, kTileN * 128, 1024);   // dS, MN-major (dQ)
+      // slot s of the Q and dO rings: the slot-0 descriptor plus s tiles
+      // (the start-address field counts 16-byte units and cannot overflow
+      // inside the 227 KB of shared memory)
+      const uint64_t q_desc0 = make_sdesc(q_s(0), 16, 1024);
+      const uint64_t q_desc0_mn = make_sdesc(q_s(0), kTileM * 128, 1024);
+      const uint64_t do_desc0 = make_sdesc(do_s(0), 16, 1024);
+      const uint64_t do_desc0_mn = make_sdesc(do_s(0), kTileM * 128, 1024);
+      constexpr uint64_t kSlot = Cfg::kTileBytes >> 4;
+      auto q_desc = [&](int s) { return q_desc0 + s * kSlot; };
+      auto q_desc_mn = [&](int s) { return q_desc0_mn + s * kSlot; };
+      auto do_desc = [&](int s) { return do_desc0 + s * kSlot; };
+      auto do_desc_mn = [&](int s) { return do_desc0_mn + s * kSlot; };
+      constexpr int kCB = kTileN * 128;   // bytes of one 64-column chunk of a 128-row tile
+
+      auto issue_s = [&](int st) {   // S^T = K_j Q_i^T, both K-major
+        mma_ss_product<D / 16, true, kCB, true, kCB>(t_s, k_desc, q_desc(st), idesc_s, 0);
         tc_commit(s_full);
       };
-      auto issue_dp = [&](int st) {   // dP^T = V_j dO_i^T
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * (kTileM * 128) + (ks % 4) * 32;
-          mma_ss(t_dp, make_sdesc(v_s + off, 16, 1024), make_sdesc(do_s(st) + off, 16, 1024),
-                 idesc_s, ks > 0);
-        }
+      auto issue_dp = [&](int st) {   // dP^T = V_j dO_i^T, both K-major
+        mma_ss_product<D / 16, true, kCB, true, kCB>(t_dp, v_desc, do_desc(st), idesc_s, 0);
         tc_commit(dp_full);
       };
 
@@ -364,21 +377,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait(p_full, n & 1, abort_flag, p.status))) break;
         tr(1);
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kTileM / 16; ++ks)
-          mma_ts(t_dv, t_s + ks * 8 + (ks >= 4 ? 64 : 0),
-                 make_sdesc(do_s(sd) + ks * 2048, kTileM * 128, 1024), idesc_kv,
-                 (n > 0 || ks > 0) ? 1u : 0u);
+        mma_ts_product8<false, 0, 64>(t_dv, t_s, do_desc_mn(sd), idesc_kv, n > 0 ? 1u : 0u);
         tc_commit(dv_done);
         tc_commit(do_empty(sd));
         // dQ (into dP^T's columns: the compute warps have read dP^T(n))
         if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, p.status))) break;
         tr(3);
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kTileN / 16; ++ks)   // dQ = dS K_j, both operands MN-major
-          mma_ss(t_dp, make_sdesc(ds_s + ks * 2048, kTileN * 128, 1024),
-                 make_sdesc(k_s + ks * 2048, kTileN * 128, 1024), idesc_q, ks > 0);
+        // dQ = dS K_j, both operands MN-major
+        mma_ss_product<kTileN / 16, false, 0, false, 0>(t_dp, ds_desc_mn, k_desc_mn, idesc_q, 0);
         tc_commit(dq_full);
         // S^T for the next step, once dV(n) has consumed P^T(n)
         if (more) {
@@ -391,11 +398,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           issue_s(st1);
         }
         // dK += dS^T Q_i; then dS^T and stage st (Q_i, dO_i) are free
-#pragma unroll
-        for (int ks = 0; ks < kTileM / 16; ++ks)
-          mma_ss(t_dk, make_sdesc(ds_s + (ks / 4) * (kTileN * 128) + (ks % 4) * 32, 16, 1024),
-                 make_sdesc(q_s(st) + ks * 2048, kTileM * 128, 1024), idesc_kv,
-                 (n > 0 || ks > 0) ? 1u : 0u);
+        mma_ss_product<kTileM / 16, true, kCB, false, 0>(t_dk, ds_desc, q_desc_mn(st), idesc_kv,
+                                                        n > 0 ? 1u : 0u);
         tc_commit(ds_empty);
         tc_commit(q_empty(st));
         tr(6);

@@ -298,8 +298,9 @@ __device__ __forceinline__ void mma_ss_product(uint32_t d_tmem, uint64_t a0, uin
 }
 
 // D (+)= A B with A in tensor memory (16-bit, two per column: step ks reads
-// columns a_tmem + 8*ks) and B in shared memory; 8 K-steps.
-template <bool kBK, int kBC>
+// columns a_tmem + 8*ks, plus kAJump further for steps 4-7) and B in shared
+// memory; 8 K-steps.
+template <bool kBK, int kBC, int kAJump = 0>
 __device__ __forceinline__ void mma_ts_product8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
                                                 uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -312,18 +313,19 @@ __device__ __forceinline__ void mma_ts_product8(uint32_t d_tmem, uint32_t a_tmem
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
       "add.s32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+      "add.s32 a, %1, %12;\n\tadd.s64 b, %2, %8;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+      "add.s32 a, %1, %13;\n\tadd.s64 b, %2, %9;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+      "add.s32 a, %1, %14;\n\tadd.s64 b, %2, %10;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+      "add.s32 a, %1, %15;\n\tadd.s64 b, %2, %11;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate),
       "n"(desc_step<kBK, kBC>(1)), "n"(desc_step<kBK, kBC>(2)), "n"(desc_step<kBK, kBC>(3)),
       "n"(desc_step<kBK, kBC>(4)), "n"(desc_step<kBK, kBC>(5)), "n"(desc_step<kBK, kBC>(6)),
-      "n"(desc_step<kBK, kBC>(7))
+      "n"(desc_step<kBK, kBC>(7)), "n"(32 + kAJump), "n"(40 + kAJump), "n"(48 + kAJump),
+      "n"(56 + kAJump)
       : "memory");
 }
 

@@ -224,6 +224,29 @@ def test_jacobian_vector_product_brute_force():
             for c in range(6):
                 J[a, c] = p[i, a] * ((a == c) - p[i, c])   # d p_a / d s_c
         assert np.abs(ds[i] - J.T @ dp[i]).max() <= 1e-15
+        # the oracle's explicit Jacobian is the same matrix
+        assert np.abs(oa.softmax_jacobian(p[i]) - J).max() <= 1e-15
+
+
+# 6e. the explicit softmax Jacobian against central finite differences of a
+#     library softmax (scipy), at random score rows including a masked entry
+def test_softmax_jacobian_finite_differences():
+    from scipy.special import softmax
+    rng = np.random.default_rng(77)
+    eps = 1e-6
+    for n in (1, 2, 5, 9):
+        s = rng.standard_normal(n) * 2.0
+        if n > 2:
+            s[-1] = -np.inf            # a masked key: its probability and derivatives are 0
+        fin = np.isfinite(s)
+        J_fd = np.zeros((n, n))
+        for c in np.flatnonzero(fin):
+            e = np.zeros(n)
+            e[c] = eps
+            J_fd[:, c] = (softmax(s + e) - softmax(s - e)) / (2 * eps)
+        J = oa.softmax_jacobian(softmax(s))
+        assert np.abs(J - J_fd).max() <= 1e-9, n
+        assert np.abs(J.sum(axis=0)).max() <= 1e-15   # columns sum to 0 (probabilities sum to 1)
 
 
 # 7. sampled-row and sampled-column evaluators agree with the dense oracle
@@ -272,6 +295,7 @@ def _pins_pass():
             test_matches_torch_sdpa_float64((1, 2, 2, 40, 8), causal)
         test_finite_differences(1, 2, 1, 5, 4, True)
         test_kv_offset_matches_torch_lower_right_bias((1, 2, 1, 5, 12, 4), True)
+        test_softmax_jacobian_finite_differences()
     except Exception:   # a failed assertion, or NaNs tripping a comparison
         return False
     return True
@@ -297,6 +321,10 @@ def test_planted_mistakes_are_caught(monkeypatch):
         "Jacobian term dropped": ("_jacobian_vjp", lambda p, dp: p * dp),
         "Jacobian sign flipped": ("_jacobian_vjp",
             lambda p, dp: p * dp + p * (p * dp).sum(axis=1, keepdims=True)),
+        "explicit Jacobian sign flipped": ("softmax_jacobian",
+            lambda p: np.diag(p) + np.outer(p, p)),
+        "explicit Jacobian diagonal dropped": ("softmax_jacobian",
+            lambda p: -np.outer(p, p)),
         "logsumexp missing the max term": ("_softmax_rows",
                                            _softmax_rows_lse_without_max),
     }
