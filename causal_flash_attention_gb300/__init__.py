@@ -16,6 +16,7 @@ loading it raises if it has not been built.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -116,6 +117,14 @@ def _dims_kv(q, k):
     return int(B), int(Hq), int(Hkv), int(Sq), int(Skv), int(d)
 
 
+def _on_device(t):
+    """Make t's GPU the current device for the call: the library runs on the
+    current device, and the default stream is taken on it."""
+    if t is not None and t.is_cuda:
+        return torch.cuda.device(t.device)
+    return contextlib.nullcontext()
+
+
 def _check_contig(*ts):
     for t in ts:
         if t is not None and not t.is_contiguous():
@@ -127,8 +136,9 @@ def fa_fwd(q, k, v, out, lse, causal=True, scale=None, stream=None):
     _check_contig(q, k, v, out, lse)
     B, Hq, Hkv, S, d = _dims(q, k)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, d,
-                      int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), _stream(stream))
+    with _on_device(q):
+        rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, d,
+                          int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_fwd")
 
@@ -145,9 +155,10 @@ def fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale=No
     B, Hq, Hkv, S, d = _dims(q, k)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
-                      _ptr(dk), _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale,
-                      DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes, _stream(stream))
+    with _on_device(q):
+        rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale,
+                          DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes, _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_bwd")
 
@@ -158,9 +169,10 @@ def fa_fwd_kv(q, k, v, out, lse, causal=True, scale=None, stream=None):
     _check_contig(q, k, v, out, lse)
     B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = lib().fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv,
-                         d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
-                         _stream(stream))
+    with _on_device(q):
+        rc = lib().fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                             d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
+                             _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_fwd_kv")
 
@@ -176,10 +188,11 @@ def fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale
     B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
-                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)), scale,
-                         DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes,
-                         _stream(stream))
+    with _on_device(q):
+        rc = lib().fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)), scale,
+                             DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes,
+                             _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_bwd_kv")
 
@@ -197,9 +210,10 @@ def fa_fwd_splitkv(q, k, v, out, lse, causal=True, scale=None, n_splits=0, works
     B, Hq, Hkv, Sq, Skv, d = _dims_kv(q, k)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
-                              Skv, d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
-                              int(n_splits), _ptr(workspace), ws_bytes, _stream(stream))
+    with _on_device(q):
+        rc = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
+                                  Skv, d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
+                                  int(n_splits), _ptr(workspace), ws_bytes, _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_fwd_splitkv")
 
@@ -230,11 +244,12 @@ def fa_fwd_splitkv_paged(q, k_cache, v_cache, block_table, out, lse, Skv, causal
     num_blocks, Hkv, block_size = (int(x) for x in k_cache.shape[:3])
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().fa_fwd_splitkv_paged(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(out), _ptr(lse), B, Hq,
-        Hkv, Sq, int(Skv), d, block_size, num_blocks, int(block_table.shape[1]),
-        int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), int(n_splits), _ptr(workspace),
-        ws_bytes, _stream(stream))
+    with _on_device(q):
+        rc = lib().fa_fwd_splitkv_paged(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(out), _ptr(lse), B, Hq,
+            Hkv, Sq, int(Skv), d, block_size, num_blocks, int(block_table.shape[1]),
+            int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), int(n_splits), _ptr(workspace),
+            ws_bytes, _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_fwd_splitkv_paged")
 
@@ -309,8 +324,9 @@ def fa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, causal=True, scale=None,
     _check_contig(q, k, v, out, dout, lse, dq, dk, dv)
     B, Hq, Hkv, S, d = _dims(q, k)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
-            _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
-            _stream(stream))
+    with _on_device(q):   # the scratch array used is the current device's
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale,
+                DTYPE_CODES.get(q.dtype, -1), _stream(stream))
     if rc != 0:
         raise FAError(rc, "fa_bwd_noalloc")

@@ -1,7 +1,18 @@
 """Build libfa.so in-tree: nvcc for sm_103a only, one object per source file,
 compiled in parallel, linked with the static CUDA runtime.
 
-    python -m causal_flash_attention_gb300.build
+    python -m causal_flash_attention_gb300.build            # libfa.so
+    python -m causal_flash_attention_gb300.build --all      # + libfa_waittest.so
+
+Variants (the same sources with one extra define each, never loaded by the
+product path):
+  trace     libfa_trace.so: kernels record per-role timelines into a buffer
+            set with its extra export fa_trace_set(void*) (FA_TRACE).
+  waittest  libfa_waittest.so: the bounded-wait limit shortened to about a
+            millisecond and every tensor-core kernel made to wait first for a
+            barrier phase that nothing completes (FA_WAIT_TEST), so that a test
+            can check that a wait which runs out ends the kernel with an error
+            status instead of a hang.
 """
 from __future__ import annotations
 
@@ -21,6 +32,13 @@ HEADERS = ["ptx.cuh", "fa_internal.h", "fa_decode.h", os.path.join("..", "..", "
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr"]
+# ~1 ms at the GB300's SM clock
+WAIT_TEST_LIMIT_CYCLES = 2_000_000
+VARIANTS = {
+    "": [],
+    "trace": ["-DFA_TRACE"],
+    "waittest": ["-DFA_WAIT_TEST", f"-DFA_WAIT_LIMIT_CYCLES={WAIT_TEST_LIMIT_CYCLES}LL"],
+}
 
 
 def nvcc() -> str:
@@ -37,53 +55,77 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False,
-          trace: bool = False) -> str:
-    """Compile and link libfa.so; returns its path. Raises on compiler errors.
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else LIB.replace("libfa.so", f"libfa_{variant}.so")
 
-    trace=True builds libfa_trace.so instead: the same library compiled with
-    FA_TRACE, whose kernels record per-role timelines into a buffer set with
-    its extra export fa_trace_set(void*). The product library never has it.
-    """
-    bdir = BUILD + ("_trace" if trace else "")
-    lib = LIB.replace("libfa.so", "libfa_trace.so") if trace else LIB
-    os.makedirs(bdir, exist_ok=True)
+
+def _paths(variant: str):
+    bdir = BUILD + (f"_{variant}" if variant else "")
+    return bdir, lib_path(variant)
+
+
+def build_variants(variants, verbose: bool = False, force: bool = False,
+                   ptxas_verbose: bool = False) -> list:
+    """Compile every stale object of the given variants in one parallel pool,
+    then link each library; returns the library paths. Raises on errors."""
     cc = nvcc()
     headers = [os.path.join(CSRC, h) for h in HEADERS]
     jobs = []
-    for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(bdir, src.replace(".cu", ".o"))
-        if force or _stale(o, [s] + headers):
-            cmd = [cc, *ARCH, *CFLAGS, *(["-DFA_TRACE"] if trace else []), "-c", s, "-o", o]
-            if ptxas_verbose:
-                cmd += ["-Xptxas", "-v"]
-            jobs.append(cmd)
-    objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
+    for variant in variants:
+        bdir, _ = _paths(variant)
+        os.makedirs(bdir, exist_ok=True)
+        for src in SOURCES:
+            s = os.path.join(CSRC, src)
+            o = os.path.join(bdir, src.replace(".cu", ".o"))
+            if force or _stale(o, [s] + headers):
+                cmd = [cc, *ARCH, *CFLAGS, *VARIANTS[variant], "-c", s, "-o", o]
+                if ptxas_verbose:
+                    cmd += ["-Xptxas", "-v"]
+                jobs.append(cmd)
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
         return cmd, r
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), 32))) as ex:
         for cmd, r in ex.map(run, jobs):
             if verbose or ptxas_verbose or r.returncode != 0:
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    if force or jobs or _stale(lib, objs):
-        tmp = lib + ".tmp"
-        cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lrt",
-               "-lpthread"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if verbose or r.returncode != 0:
-            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-        if r.returncode != 0:
-            raise RuntimeError(f"link of {os.path.basename(lib)} failed")
-        os.replace(tmp, lib)
-    return lib
+    libs = []
+    for variant in variants:
+        bdir, lib = _paths(variant)
+        objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
+        if force or _stale(lib, objs):
+            tmp = lib + ".tmp"
+            cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lrt",
+                   "-lpthread"]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if verbose or r.returncode != 0:
+                sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+            if r.returncode != 0:
+                raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+            os.replace(tmp, lib)
+        libs.append(lib)
+    return libs
+
+
+def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False,
+          trace: bool = False, variant: str = "") -> str:
+    """Compile and link libfa.so (or the named variant); returns its path."""
+    v = "trace" if trace else variant
+    return build_variants([v], verbose, force, ptxas_verbose)[0]
+
+
+def build_all(verbose: bool = False, force: bool = False) -> list:
+    """The product library and the wait-limit test library, compiled together."""
+    return build_variants(["", "waittest"], verbose, force)
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv,
-                trace="--trace" in sys.argv))
+    if "--all" in sys.argv:
+        print(build_all(verbose=True, force="--force" in sys.argv))
+    else:
+        print(build(verbose=True, force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv,
+                    trace="--trace" in sys.argv))

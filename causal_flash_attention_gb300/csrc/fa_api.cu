@@ -162,6 +162,20 @@ SplitPlan split_plan(int B, int Hq, int Hkv, int Sq, int Skv, int d, int n_split
 }
 
 }  // namespace
+
+int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
+                   const void* dout, const float* lse, const void* dq, const void* dk,
+                   const void* dv, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                   float scale, int dtype) {
+  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -260,12 +274,9 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
               int Skv, int d, int causal, float scale, int dtype, void* workspace,
               size_t workspace_bytes, fa_stream_t stream) {
-  int rc = check_common(B, Hq, Hkv, Sq, Skv, d, causal, scale, dtype);
+  int rc = check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Skv, d, causal,
+                          scale, dtype);
   if (rc != FA_OK) return rc;
-  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_ALIGN;
   const WsLayout ws = ws_layout(B, Hq, Sq, d);
   if (!workspace || workspace_bytes < ws.total) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;

@@ -70,7 +70,7 @@ struct DecCfg {
 __device__ __forceinline__ void drain_wait_d(uint32_t bar, uint32_t parity, int* status) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > kDrainLimitCycles) {
       atomicOr(status, kStatusWaitTimeout);
       return;
     }
@@ -224,6 +224,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       };
       bool ok = mbar_wait(q_ready, 0, abort_flag, p.status) &&
                 mbar_wait(k_full(0), 0, abort_flag, p.status);
+#ifdef FA_WAIT_TEST
+      // wait-limit test build: nothing completes this phase before the abort
+      // path's own commit, so the wait runs out
+      if (ok) ok = mbar_wait(drain, 0, abort_flag, p.status);
+#endif
       if (ok) {
         tc_fence_after();
         issue_qk(0);

@@ -84,7 +84,7 @@ struct FwdBars {
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > kDrainLimitCycles) {
       atomicOr(status, kStatusWaitTimeout);
       return;
     }
@@ -216,6 +216,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc_qk = make_idesc(128, kTileN, kBf16, false, false);
       constexpr uint32_t idesc_pv = make_idesc(128, D, kBf16, false, true);
       bool ok = mbar_wait(bars.q_full, 0, abort_flag, p.status);
+#ifdef FA_WAIT_TEST
+      // wait-limit test build: nothing completes this phase before the abort
+      // path's own commit, so the wait runs out
+      if (ok) ok = mbar_wait(bars.drain, 0, abort_flag, p.status);
+#endif
 
       auto issue_qk = [&](int t, int st) {   // S_t = Q_t K^T, both K-major
         const uint64_t qa = make_sdesc(sbase + Cfg::kOffQ + t * Cfg::kTileBytes, 16, 1024);

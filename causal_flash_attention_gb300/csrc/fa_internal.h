@@ -84,6 +84,14 @@ struct SimtParams {
   float scale;
 };
 
+// Host-side argument checks of the backward entry points (shapes, dtype,
+// scale, null and 16-byte alignment of every pointer); FA_OK or an FA_ERR_*
+// code. Defined in fa_api.cu.
+int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
+                   const void* dout, const float* lse, const void* dq, const void* dk,
+                   const void* dv, int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                   float scale, int dtype);
+
 // Launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);

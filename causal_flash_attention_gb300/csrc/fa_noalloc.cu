@@ -57,14 +57,14 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
                               int B, int Hq, int Hkv, int S, int d, int causal, float scale,
                               int dtype, fa_stream_t stream) {
-  const size_t need = fa_bwd_workspace_bytes(B, Hq, Hkv, S, d);
-  if (need > fa::kScratchBytes) return FA_ERR_NOALLOC_LIMIT;
-  // need == 0 means invalid sizes: fa_bwd reports the exact argument error.
-  void* scratch = nullptr;
-  if (need > 0) {
-    scratch = fa::scratch_on_current_device();
-    if (!scratch) return FA_ERR_CUDA;
-  }
+  // the argument errors of fa_bwd first, then the scratch limit; neither
+  // failure looks up or touches the scratch array
+  const int rc = fa::check_bwd_args(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, S, S, d,
+                                    causal, scale, dtype);
+  if (rc != FA_OK) return rc;
+  if (fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) > fa::kScratchBytes) return FA_ERR_NOALLOC_LIMIT;
+  void* scratch = fa::scratch_on_current_device();
+  if (!scratch) return FA_ERR_CUDA;
   return fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, S, d, causal, scale, dtype,
                 scratch, fa::kScratchBytes, stream);
 }

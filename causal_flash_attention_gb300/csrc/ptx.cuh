@@ -21,7 +21,18 @@ enum : int {
 
 // A healthy wait finishes in microseconds; this bound (about two seconds at
 // the GB300's SM clock) only ends a wait that would otherwise never finish.
+// The waits of the abort path (for copies and MMAs already issued, which
+// always complete) use kDrainLimitCycles instead. A wait-limit test build of
+// the library (FA_WAIT_TEST) shortens the first bound only and makes each
+// kernel's MMA issuer start by waiting for a barrier phase that nothing
+// completes, so that its bounded wait runs out and the kernel takes the
+// abort path and reports kStatusWaitTimeout.
+#ifdef FA_WAIT_LIMIT_CYCLES
+constexpr long long kWaitLimitCycles = FA_WAIT_LIMIT_CYCLES;
+#else
 constexpr long long kWaitLimitCycles = 4000000000LL;
+#endif
+constexpr long long kDrainLimitCycles = 4000000000LL;
 
 // ----------------------------------------------------------------- trace --
 // Timeline tracing, compiled in only when FA_TRACE is defined (a separate
@@ -478,7 +489,6 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 
-// Named barrier among `nthreads` threads (a multiple of 32).
 // 16-byte store to a shared-memory address
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -487,6 +497,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Named barrier among `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

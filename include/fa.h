@@ -195,7 +195,9 @@ int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache
 /*
  * Size of the fixed device scratch array behind fa_bwd_noalloc (32 MiB). A
  * call fits when fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) is at most this,
- * e.g. B*Hq = 96 heads at S = 1024, d = 64 (about 25.9 MB).
+ * e.g. B*Hq = 96 heads at S = 1024, d = 64 (about 25.9 MB). The limit uses
+ * that one size for every dtype, although FA_F32 calls use only the D and
+ * LSE rows of it.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -203,21 +205,28 @@ int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache
  * Backward pass for callers that cannot allocate device memory (for example
  * code inside a framework or plugin callback that owns every device
  * allocation, or latency-critical code that must not call cudaMalloc/cudaFree
- * because they can synchronize the device). Same arguments, results and
- * errors as fa_bwd, without the workspace: the scratch is a fixed
+ * because they can synchronize the device). Same arguments and results as
+ * fa_bwd, without the workspace: the scratch is a fixed
  * FA_NOALLOC_SCRATCH_BYTES array in the library's device memory, held on every
  * GPU that loads the library until the process exits. The call allocates
  * nothing. This entry point has no counterpart in the method's description;
  * it is a deployment aid.
  *
- * Limits and sharing: returns FA_ERR_NOALLOC_LIMIT, having enqueued nothing,
- * when the sizes need more scratch than FA_NOALLOC_SCRATCH_BYTES. The first
- * call made with a given device current looks up the array's device address
- * on that device; make that first call before any stream capture. Every call
- * shares the one array and it keeps the last call's contents (each call
- * rewrites all of it that it reads, so results do not depend on them). Calls
- * whose work overlaps on the GPU (unordered streams, concurrent host threads)
- * race on the array: the caller must order them.
+ * Errors: first fa_bwd's argument errors (FA_ERR_SHAPE, FA_ERR_DTYPE,
+ * FA_ERR_SCALE, FA_ERR_NULL, FA_ERR_ALIGN), then FA_ERR_NOALLOC_LIMIT when
+ * the sizes need more scratch than FA_NOALLOC_SCRATCH_BYTES; either way
+ * nothing is enqueued and the scratch array is not looked up.
+ *
+ * Device and set-up: the array used is the current device's, so the current
+ * device must be the one that owns `stream` and every pointer. The first call
+ * that passes the checks with a given device current looks up the array's
+ * device address on that device; make that first call before any stream
+ * capture.
+ *
+ * Sharing: every call shares the one array and it keeps the last call's
+ * contents (each call rewrites all of it that it reads, so results do not
+ * depend on them). Calls whose work overlaps on the GPU (unordered streams,
+ * concurrent host threads) race on the array: the caller must order them.
  */
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
                    const void* dout, const float* lse, void* dq, void* dk, void* dv,

@@ -168,7 +168,8 @@ def test_repeat_calls_same_result(fa):
 # ------------------------------------------------------------ large sizes --
 def test_longest_sequence_sampled(fa):
     """S = 65536 (twice the longest workload), one head, d = 64: forward and dQ
-    on sampled rows (dK/dV would need every row in the oracle)."""
+    on sampled query rows, dK and dV on sampled key rows (the oracle evaluates
+    every query row for those, streaming 512 rows at a time)."""
     B, H, S, d = 1, 1, 65536, 64
     q, k, v, do = fa_inputs.make_custom(B, H, H, S, d, "bf16", seed=65)
     scale = 1.0 / math.sqrt(d)
@@ -180,6 +181,10 @@ def test_longest_sequence_sampled(fa):
     assert np.abs(got["lse"][0, 0, rows] - l_r).max() <= LSE_TOL
     check_grad("dq", got["dq"][0, 0, rows], dq_r)
     assert np.isfinite(got["dk"]).all() and np.isfinite(got["dv"]).all()
+    keys = fa_inputs.sample_rows(S, 32, seed=67)
+    dk_c, dv_c = oracle.key_columns(Q, K, V, DO, 0, 0, keys, True, scale)
+    check_grad("dk", got["dk"][0, 0, keys], dk_c)
+    check_grad("dv", got["dv"][0, 0, keys], dv_c)
 
 
 def test_many_heads_gqa(fa):
