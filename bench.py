@@ -281,6 +281,111 @@ def job_tflops(flops_per_rank_step, world, ms_per_step):
     return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
 
 
+# ------------------------------------------------------- other workloads --
+# Timed after the headline workload in the default run, each on its own inputs
+# with its own warm-up: the other shapes the metric is quoted on (d = 64 and
+# short sequences, grouped-query heads, fp16 at 32K positions) and the
+# unmasked, chunked-prefill, decode and paged-decode rows.
+PER_CONFIG = ["gpt2_small", "gqa_qwen3", "fp16_32k", "gqa_qwen3_nc", "long_8k_nc", "prefill_8k",
+              "decode_8k", "spec_32k", "decode_8k_paged"]
+
+
+def _calls_for(fa, w, dev):
+    """(fwd(), bwd() or None, input bytes) for workload w on fresh device
+    buffers; the same entry points run_gpu times."""
+    import torch
+    q, k, v, do = fa_inputs.make_inputs(w)
+    table = None
+    if w.page_size:
+        k, v, table, _ = fa_inputs.make_paged(k, v, w.page_size, seed=w.page_size)
+        table = table.to(dev)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    out = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
+    nbytes = sum(x.numel() * x.element_size() for x in (qd, kd, vd, dod))
+    if w.decode:
+        n = fa.fa_fwd_splitkv_workspace_bytes(w.B, w.Hq, w.Hkv, w.S, w.kv_len, w.d, 0)
+        ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+        if w.page_size:
+            fwd = lambda: fa.fa_fwd_splitkv_paged(qd, kd, vd, table, out, lse, w.kv_len, w.causal,
+                                                  w.scale, 0, ws)
+        else:
+            fwd = lambda: fa.fa_fwd_splitkv(qd, kd, vd, out, lse, w.causal, w.scale, 0, ws)
+        return fwd, None, nbytes
+    same = w.S == w.kv_len
+    fwd = (lambda: fa.fa_fwd(qd, kd, vd, out, lse, w.causal, w.scale)) if same else \
+        (lambda: fa.fa_fwd_kv(qd, kd, vd, out, lse, w.causal, w.scale))
+    if not w.backward:
+        return fwd, None, nbytes
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = fa.workspace_for(qd, kd)
+    bwd = (lambda: fa.fa_bwd(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale)) \
+        if same else \
+        (lambda: fa.fa_bwd_kv(qd, kd, vd, out, dod, lse, dq, dk, dv, ws, w.causal, w.scale))
+    fwd()
+    return fwd, bwd, nbytes
+
+
+def time_config(fa, w, dev, peaks, warm=10, calls=30):
+    """Per-call CUDA-event times (median over `calls`) of the workload's
+    forward and backward entry points, with its roofline against the measured
+    peaks. Inputs smaller than L2 get an L2 flush (a 256 MiB write) before
+    every timed call; larger ones need none."""
+    import torch
+    fwd, bwd, nbytes = _calls_for(fa, w, dev)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if nbytes <= L2_BYTES else None
+    res = {"workload": w.describe(),
+           "l2": "flushed before every timed call" if flush is not None else
+                 f"inputs ({nbytes / 2**20:.0f} MiB) larger than L2; no flush"}
+    peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    for name, fn, fl, nb in (("fwd", fwd, flops(w, True, False), fwd_algorithmic_bytes(w)),
+                             ("bwd", bwd, flops(w, False, True), bwd_algorithmic_bytes(w))):
+        if fn is None:
+            continue
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(calls):
+            if flush is not None:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        entry = {"ms": ms, "ms_mean": statistics.mean(ts)}
+        if w.decode:   # HBM-bound: the split-KV forward streams K and V once
+            gbs = nb / (ms * 1e-3) / 1e9
+            entry.update({"bound": "hbm", "achieved_gbs": gbs, "frac": gbs / hbm,
+                          "peak_gbs": hbm})
+        else:
+            tf = fl / (ms * 1e-3) / 1e12
+            entry.update({"bound": "tensor", "tflops": tf, "frac": tf / peak,
+                          "hbm_side": hbm_side(nb, fl, ms, peak, hbm)})
+        res[name] = entry
+    torch.cuda.synchronize(dev)
+    return res
+
+
+def time_sustained(step, dev, stream, seconds, ms_per_step, local_rank):
+    """Back-to-back steps for about `seconds`, timed with CUDA events around
+    the whole run, clocks sampled meanwhile."""
+    import torch
+    n = max(10, int(seconds * 1e3 / max(ms_per_step, 1e-3)))
+    with ClockSampler(local_rank) as clocks:
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+    return n, a.elapsed_time(b), clocks.summary()
+
+
 # ---------------------------------------------------------------- GPU arm --
 def run_gpu(args, w, rank, world, local_rank):
     import torch
@@ -450,12 +555,26 @@ def run_gpu(args, w, rank, world, local_rank):
     if status:
         raise RuntimeError(f"device status {status} in the timed region")
 
+    sustained = None
+    if args.sustain_s > 0:
+        n_s, ms_s, clk_s = time_sustained(step, dev, stream, args.sustain_s, total_ms / K, local_rank)
+        sustained = {"steps": n_s, "total_ms": ms_s, "clocks": clk_s}
+    per_config = {}
+    if not args.no_per_config and w.name == "long_8k" and not args.heads:
+        peaks, _ = load_peaks()
+        for name in PER_CONFIG:
+            per_config[name] = time_config(fa, fa_inputs.WORKLOADS[name], dev, peaks)
+    status = fa.fa_last_device_status(stream)
+    if status:
+        raise RuntimeError(f"device status {status} in the sustained or per-workload timing")
+
     total_ms, fwd_ms, bwd_ms, e2e_ms, fwd_med, bwd_med = max_over_ranks(
         [total_ms, fwd_ms, bwd_ms, e2e_ms, fwd_med, bwd_med], dist, dev)
     return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms,
                 fwd_med_ms=fwd_med, bwd_med_ms=bwd_med,
                 h2d=h2d, d2h=d2h, link=link, clocks=clocks.summary(), dist=dist,
-                launches_per_fwd=(2 if dec_ws_bytes else 1))
+                launches_per_fwd=(2 if dec_ws_bytes else 1), sustained=sustained,
+                per_config=per_config)
 
 
 def main():
@@ -467,6 +586,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer timing")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps timed after the main region (0: skip)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other workloads after long_8k")
     ap.add_argument("--heads", type=int, default=0,
                     help="override Hq (and Hkv in the same ratio): a smaller case of the same "
                          "workload, e.g. for profiler captures")
@@ -592,6 +715,23 @@ def main():
         "gpu_launches": (r["launches_per_fwd"] + (3 if w.backward else 0)) * K,
         "clocks": r["clocks"],
     }
+    if r["sustained"]:
+        sus = r["sustained"]
+        sus_ms = sus["total_ms"] / sus["steps"]
+        sus_tf = job_tflops(step_flops, world, sus_ms)
+        mhz = sus["clocks"]["sm_mhz"]
+        line["sustained"] = {
+            "steps": sus["steps"], "seconds": sus["total_ms"] / 1e3, "ms_per_step": sus_ms,
+            "tflops": sus_tf, "frac_of_sustained_peak": sus_tf / world / peaks["bf16_tflops_sustained"],
+            "sustained_peak_tflops": peaks["bf16_tflops_sustained"],
+            "frac_of_burst_peak": sus_tf / world / peak,
+            "clocks": sus["clocks"],
+            "ms_x_median_mhz": sus_ms * mhz if mhz else None,
+            "burst_ms_x_median_mhz": ms_per_step * r["clocks"]["sm_mhz"] if r["clocks"]["sm_mhz"] else None,
+            "note": "back-to-back steps after the burst region; CUDA events around the whole run",
+        }
+    if r["per_config"]:
+        line["per_config"] = r["per_config"]
     if not w.backward:   # forward-only workload: the forward kernel is the whole step
         line["roofline"] = dict(line["roofline_fwd"])
     if w.decode:
