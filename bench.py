@@ -326,7 +326,7 @@ def _calls_for(fa, w, dev):
     return fwd, bwd, nbytes
 
 
-def time_config(fa, w, dev, peaks, warm=10, calls=30):
+def time_config(fa, w, dev, peaks, warm=10, calls=30, forward_only=False):
     """Per-call CUDA-event times (median over `calls`) of the workload's
     forward and backward entry points, with its roofline against the measured
     peaks. Inputs smaller than L2 get an L2 flush (a 256 MiB write) before
@@ -338,6 +338,8 @@ def time_config(fa, w, dev, peaks, warm=10, calls=30):
            "l2": "flushed before every timed call" if flush is not None else
                  f"inputs ({nbytes / 2**20:.0f} MiB) larger than L2; no flush"}
     peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    if forward_only:
+        bwd = None
     for name, fn, fl, nb in (("fwd", fwd, flops(w, True, False), fwd_algorithmic_bytes(w)),
                              ("bwd", bwd, flops(w, False, True), bwd_algorithmic_bytes(w))):
         if fn is None:
@@ -564,6 +566,18 @@ def run_gpu(args, w, rank, world, local_rank):
         peaks, _ = load_peaks()
         for name in PER_CONFIG:
             per_config[name] = time_config(fa, fa_inputs.WORKLOADS[name], dev, peaks)
+        # the CTA-pair forward (tcgen05 cta_group::2) on the headline shape, for
+        # comparison with the single-CTA forward that fa_fwd runs by default
+        prev = os.environ.get("FA_FWD_CTA_PAIR")
+        os.environ["FA_FWD_CTA_PAIR"] = "1"
+        try:
+            per_config["long_8k_cta_pair_forward"] = time_config(
+                fa, fa_inputs.WORKLOADS["long_8k"], dev, peaks, forward_only=True)
+        finally:
+            if prev is None:
+                del os.environ["FA_FWD_CTA_PAIR"]
+            else:
+                os.environ["FA_FWD_CTA_PAIR"] = prev
     status = fa.fa_last_device_status(stream)
     if status:
         raise RuntimeError(f"device status {status} in the sustained or per-workload timing")

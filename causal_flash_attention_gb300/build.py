@@ -26,7 +26,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_simt.cu", "fa_noalloc.cu", "fa_decode.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_pair.cu", "fa_bwd.cu", "fa_simt.cu", "fa_noalloc.cu",
+           "fa_decode.cu"]
 HEADERS = ["ptx.cuh", "fa_internal.h", "fa_decode.h", os.path.join("..", "..", "include", "fa.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/fa.h"
@@ -111,6 +112,20 @@ int check_common(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, flo
 }
 
 inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+// Forward kernel for 16-bit inputs at d = 128: the CTA-pair kernel
+// (fa_fwd_pair.cu, tcgen05 cta_group::2) or the single-CTA one (fa_fwd.cu).
+// Both compute the same function. FA_FWD_CTA_PAIR=1 (or 0) in the environment
+// selects one for every call; otherwise kPairForwardDefault does.
+constexpr bool kPairForwardDefault = false;
+
+bool use_pair_forward(int d) {
+  if (d != 128) return false;
+  const char* e = std::getenv("FA_FWD_CTA_PAIR");
+  if (e && e[0] == '1') return true;
+  if (e && e[0] == '0') return false;
+  return kPairForwardDefault;
+}
 
 struct WsLayout {
   size_t dq_acc, delta, lse2, total;
@@ -252,6 +267,11 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* out, float* lse
   p.trace = FA_TRACE_PTR;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
+  if (use_pair_forward(d)) {
+    if (!make_tmap(&p.tm_k_half, k, B * Hkv, Skv, d, bf16, kTileN / 2)) return FA_ERR_TMA;
+    p.n_qblocks = (Sq + 4 * kTileM - 1) / (4 * kTileM);
+    return launch_fwd_pair(p, bf16, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
   return launch_fwd_tc(p, d, bf16, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -32,6 +32,9 @@ struct FwdParams {
                       // query tile qt walks is qt + kv_tiles_ahead
   int* status;        // device status word (wait timeouts)
   unsigned long long* trace;   // timeline buffer of trace builds (FA_TRACE); else null
+  // CTA-pair forward (d = 128) only:
+  CUtensorMap tm_k_half;   // k as tm_k with a box of 64 rows: each CTA of a pair loads half a tile
+  int n_qblocks;           // ceil(Sq / 512): CTA pairs per (batch, query head)
 };
 
 struct BwdPreParams {
@@ -94,6 +97,7 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* out,
 
 // Launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, bool bf16, cudaStream_t stream);
+cudaError_t launch_fwd_pair(const FwdParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_tc(const BwdParams& p, int d, bool bf16, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream);

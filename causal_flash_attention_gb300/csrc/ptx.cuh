@@ -340,6 +340,154 @@ __device__ __forceinline__ void mma_ts_product8(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// ---- CTA pairs (cta_group::2) ----------------------------------------------
+// A cluster of two CTAs on two SMs shares one instruction stream: the even
+// CTA of the pair (the leader) issues M = 256 products whose D rows 0-127 land
+// in its own tensor memory and rows 128-255 in its peer's, at the same column
+// address; A rows come from each CTA's own shared memory (or tensor memory),
+// and B's N columns are split, the first N/2 read from the leader's shared
+// memory and the rest from the peer's, at the same offset. Tensor memory is
+// allocated and freed jointly (one warp in each CTA), and every tcgen05
+// instruction of a kernel that pairs uses the cta_group::2 form.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs; orders shared-memory and barrier set-up (and the
+// final reads of the peer's memory) across the pair.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster
+// scope: this thread's prior writes and tensor-memory stores, fenced, are
+// visible to the thread that observes the phase).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for a phase that arrivals from the other CTA complete.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusWaitTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` of every CTA in `cta_mask`
+// (bit i = cluster rank i) when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Pair forms of mma_ss_product (8 K-steps) and mma_ts_product8: M = 256 across
+// the two CTAs.
+template <bool kAK, int kAC, bool kBK, int kBC>
+__device__ __forceinline__ void mma_pair_ss_product8(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %12;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %13;\n\tadd.s64 b, %2, %14;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %15;\n\tadd.s64 b, %2, %16;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %17;\n\tadd.s64 b, %2, %18;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, pt;\n\t}" ::"r"(d_tmem),
+      "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate),
+      "n"(desc_step<kAK, kAC>(1)), "n"(desc_step<kBK, kBC>(1)),
+      "n"(desc_step<kAK, kAC>(2)), "n"(desc_step<kBK, kBC>(2)),
+      "n"(desc_step<kAK, kAC>(3)), "n"(desc_step<kBK, kBC>(3)),
+      "n"(desc_step<kAK, kAC>(4)), "n"(desc_step<kBK, kBC>(4)),
+      "n"(desc_step<kAK, kAC>(5)), "n"(desc_step<kBK, kBC>(5)),
+      "n"(desc_step<kAK, kAC>(6)), "n"(desc_step<kBK, kBC>(6)),
+      "n"(desc_step<kAK, kAC>(7)), "n"(desc_step<kBK, kBC>(7))
+      : "memory");
+}
+
+template <bool kBK, int kBC>
+__device__ __forceinline__ void mma_pair_ts_product8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, pt;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate),
+      "n"(desc_step<kBK, kBC>(1)), "n"(desc_step<kBK, kBC>(2)), "n"(desc_step<kBK, kBC>(3)),
+      "n"(desc_step<kBK, kBC>(4)), "n"(desc_step<kBK, kBC>(5)), "n"(desc_step<kBK, kBC>(6)),
+      "n"(desc_step<kBK, kBC>(7))
+      : "memory");
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
 //   1 = bf16), 15 A major, 16 B major (0 = K-major, 1 = MN-major),

@@ -7,7 +7,8 @@ the library's device status word, which fa_last_device_status reads and
 clears. libfa_waittest.so is the same library built with the wait limit cut to
 about a millisecond and each tensor-core kernel's MMA issuer made to wait
 first for a barrier phase that nothing completes (built by
-causal_flash_attention_gb300.build.build_all). Nothing faults, traps or
+causal_flash_attention_gb300.build.build_all). The forward runs in both its
+single-CTA and its CTA-pair form. Nothing faults, traps or
 hangs: the wait ends at its limit. The test checks that each call returns,
 that the status reports the timeout and is cleared by the read, and that the
 product library, called next in the same process and context, still computes
@@ -15,6 +16,7 @@ results that match the oracle with a clean status.
 """
 import ctypes
 import math
+import os
 
 import numpy as np
 import pytest
@@ -74,6 +76,17 @@ def test_wait_that_runs_out_ends_the_kernel_with_an_error_status(fa):
     torch.cuda.synchronize(dev)   # the kernel ended
     assert _status(L, stream) & STATUS_WAIT_TIMEOUT
     assert _status(L, stream) == 0   # the read cleared it
+
+    # the CTA-pair forward (d = 128): both CTAs of every pair end
+    os.environ["FA_FWD_CTA_PAIR"] = "1"
+    try:
+        assert L.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(),
+                        lse.data_ptr(), B, Hq, Hkv, S, d, 1, scale, 2, stream) == 0
+        torch.cuda.synchronize(dev)
+    finally:
+        del os.environ["FA_FWD_CTA_PAIR"]
+    assert _status(L, stream) & STATUS_WAIT_TIMEOUT
+    assert _status(L, stream) == 0
 
     # backward (on the product forward's out and lse)
     ref_out, ref_lse = fa.attention_forward(qd, kd, vd, True, scale)
