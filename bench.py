@@ -108,6 +108,7 @@ def load_peaks():
 
 KERNEL_SOURCES = {"fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"),
                   "fa_bwd_kernel": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
+                  "fa_fwd_pair_kernel": ("fa_fwd_pair.cu", "ptx.cuh", "fa_internal.h"),
                   "fa_decode_kernel": ("fa_decode.cu", "ptx.cuh", "fa_internal.h", "fa_decode.h")}
 
 
