@@ -79,6 +79,13 @@ enum {
  * Forward pass. Writes out[B][Hq][S][d] (dtype) and lse[B][Hq][S] (float32,
  * natural-log logsumexp of the scaled, masked score row). causal != 0 masks
  * key positions j > i. scale is usually 1/sqrt(d).
+ *
+ * For FA_BF16 / FA_F16 at d = 128 the forward (here and in fa_fwd_kv) runs
+ * either a single-CTA kernel (the default) or a CTA-pair kernel on the
+ * tensor cores' 2-CTA mode ("Phase 14: Flash Attention 2 for SM120", section
+ * 硬件约束); both write the same bits. The environment variable
+ * FA_FWD_CTA_PAIR, read at every call, selects the pair kernel when it is "1"
+ * and the single-CTA kernel when it is "0".
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
            int B, int Hq, int Hkv, int S, int d, int causal, float scale,
