@@ -113,7 +113,11 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
+__global__ void __launch_bounds__(256, 8) bwd_pre_kernel(const BwdPreParams p) {
+  // the main kernel (launched as this grid's programmatic dependent) may be
+  // scheduled now: its prologue overlaps this pass, and it waits for this
+  // grid's completion before it reads anything this pass writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int U = p.d * static_cast<int>(sizeof(T)) / 16;   // power of two, divides 32
   const int rpw = 32 / U;
@@ -148,7 +152,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 // -------------------------------------------------------------- convert --
 // dq = scale * dq_acc (rows < Sq), 8 elements per thread.
 template <bool kBf16>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
+__global__ void __launch_bounds__(256, 8) dq_convert_kernel(const DqConvertParams p) {
+  // launched as the main kernel's programmatic dependent: wait for that grid
+  // (and the pre-pass before it) to complete and its writes to be visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long n8 = static_cast<long long>(p.BH) * p.Sq * p.d / 8;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -255,6 +262,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as the pre-pass's programmatic dependent: everything above ran
+  // alongside it; the D, L and zeroed dQ rows it writes are read below
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ===================== TMA producer =====================
@@ -620,10 +630,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // the dQ convert kernel (this grid's programmatic dependent) may be
+  // scheduled once every CTA got here; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Launch as the programmatic dependent of the kernel before it on the stream:
+// the new grid may start before that one completes and synchronizes with it
+// through griddepcontrol.wait.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int D, bool kBf16>
@@ -633,8 +665,8 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles * p.B * p.Hkv);
-  kernel<<<grid, kBwdThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  e = launch_dependent(kernel, dim3(grid), dim3(kBwdThreads), smem, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -660,9 +692,10 @@ cudaError_t launch_bwd_tc(const BwdParams& p, int d, bool bf16, cudaStream_t str
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(p.BH) * p.Sq * p.d / 8;
   const unsigned grid = static_cast<unsigned>(std::min<long long>((n8 + 255) / 256, 152LL * 16));
-  if (p.dtype == 2) dq_convert_kernel<true><<<grid, 256, 0, stream>>>(p);
-  else dq_convert_kernel<false><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e =
+      p.dtype == 2 ? launch_dependent(dq_convert_kernel<true>, dim3(grid), dim3(256), 0, stream, p)
+                   : launch_dependent(dq_convert_kernel<false>, dim3(grid), dim3(256), 0, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace fa
