@@ -249,6 +249,28 @@ def oracle_block(w, max_rows):
     return r, kv
 
 
+def oracle_one_thread(name="tiny_fp32"):
+    """Seconds and FLOPs of the fp64 oracle's dense forward + backward of a
+    whole small workload with BLAS held to one thread (a child process: the
+    thread count is fixed when numpy loads its BLAS)."""
+    code = ("import time, fa_inputs, oracle, bench\n"
+            f"w = fa_inputs.WORKLOADS[{name!r}]\n"
+            "q, k, v, do = (t.double().numpy() for t in fa_inputs.make_inputs(w))\n"
+            "oracle.forward(q, k, v, w.causal, w.scale)\n"
+            "t0 = time.perf_counter()\n"
+            "oracle.forward(q, k, v, w.causal, w.scale)\n"
+            "oracle.backward(q, k, v, do, w.causal, w.scale)\n"
+            "print(time.perf_counter() - t0, bench.flops(w, True, w.backward))\n")
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                             text=True, timeout=300)
+        sec, fl = (float(x) for x in out.stdout.split())
+        return sec, fl
+    except Exception:
+        return None, None
+
+
 def oracle_sample(w, head_inputs, block):
     """Time the fp64 oracle's dense forward + backward on `block` (rows, keys)
     of one head of workload `w`. Returns (seconds, flops of that block by the
@@ -782,6 +804,17 @@ def main():
                       f"of query heads 0 and 1 of {w.name} (all of each head when the block "
                       f"covers it): {total_f / 1e9:.1f} GFLOP by the same convention in "
                       f"{total_t:.2f} s"}
+        rate = total_f / total_t
+        line["cpu_baseline"]["extrapolated_full_step_s"] = step_flops / rate
+        line["cpu_baseline"]["extrapolation"] = (
+            f"the whole {w.name} step ({step_flops / 1e12:.2f} TFLOP) at the sampled rate: "
+            "an extrapolation, not measured")
+        sec1, fl1 = oracle_one_thread()
+        if sec1:
+            line["cpu_baseline"]["tiny_fp32_one_thread"] = {
+                "seconds": sec1, "gflop": fl1 / 1e9, "tflops": fl1 / sec1 / 1e12, "threads": 1,
+                "sample": "fp64 dense forward + softmax-Jacobian backward of the whole tiny_fp32 "
+                          "workload (fp32 B=1 Hq=Hkv=2 S=128 d=64), BLAS held to one thread"}
     if r["dist"] is not None:
         r["dist"].destroy_process_group()
     print(json.dumps(line))
