@@ -128,7 +128,7 @@ bool use_pair_forward(int d) {
 }
 
 struct WsLayout {
-  size_t dq_acc, delta, lse2, total;
+  size_t dq_acc, delta, lse2, work, total;
 };
 
 WsLayout ws_layout(int B, int Hq, int Sq, int d) {
@@ -138,7 +138,8 @@ WsLayout ws_layout(int B, int Hq, int Sq, int d) {
   w.dq_acc = 0;
   w.delta = static_cast<size_t>(round_up(bh * s_pad * d * 4, 256));
   w.lse2 = w.delta + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
-  w.total = w.lse2 + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
+  w.work = w.lse2 + static_cast<size_t>(round_up(bh * s_pad * 4, 256));
+  w.total = w.work + 256;   // the backward's work-item counter
   return w;
 }
 
@@ -321,7 +322,9 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
       (!make_tmap(&p.tm_q, q, BH, Sq, d, bf16) || !make_tmap(&p.tm_k, k, B * Hkv, Skv, d, bf16) ||
        !make_tmap(&p.tm_v, v, B * Hkv, Skv, d, bf16) ||
        !make_tmap(&p.tm_do, dout, BH, Sq, d, bf16) ||
-       !make_tmap_acc(&p.tm_dq, dq_acc, BH, Sq_pad, d)))
+       !make_tmap_acc(&p.tm_dq, dq_acc, BH, Sq_pad, d) ||
+       !make_tmap(&p.tm_dk, dk, B * Hkv, Skv, d, bf16, 32) ||
+       !make_tmap(&p.tm_dv, dv, B * Hkv, Skv, d, bf16, 32)))
     return FA_ERR_TMA;
 
   BwdPreParams pre;
@@ -331,6 +334,7 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
   pre.delta = delta;
   pre.lse2 = lse2;
   pre.dq_acc = dq_acc;
+  pre.work = dtype == FA_F32 ? nullptr : reinterpret_cast<int*>(wsb + ws.work);
   pre.BH = BH; pre.Sq = Sq; pre.Sq_pad = Sq_pad; pre.d = d;
   pre.dtype = dtype;
   if (launch_bwd_pre(pre, st) != cudaSuccess) return FA_ERR_CUDA;
@@ -356,6 +360,7 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* out, cons
   p.delta = delta;
   p.lse2 = lse2;
   p.dq_acc = dq_acc;
+  p.work = reinterpret_cast<int*>(wsb + ws.work);
   p.dk = dk;
   p.dv = dv;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.Sq_pad = Sq_pad;

@@ -7,14 +7,19 @@
 //   dQ_i = scale sum_j ds_ij K_j, dK_j = scale sum_i ds_ij Q_i, dV_j = sum_i p_ij dO_i.
 //
 // Three kernels on one stream:
-//   1. bwd_pre:    D_i, L_i * log2(e) (padded rows: D = 0, L = +inf) and a zeroed
-//                  fp32 dQ accumulator. Bandwidth-bound.
-//   2. bwd_main:   one CTA per (batch, key/value head, 128-row key tile j). K_j and
+//   1. bwd_pre:    D_i, L_i * log2(e) (padded rows: D = 0, L = +inf), a zeroed
+//                  fp32 dQ accumulator and a zeroed work-item counter.
+//                  Bandwidth-bound.
+//   2. bwd_main:   persistent, one CTA per SM. A work item is one (batch, key/value
+//                  head, 128-row key tile j); CTAs claim items from the counter,
+//                  lowest j (most work under the causal mask) first. K_j and
 //                  V_j stay in shared memory, dK_j and dV_j stay in tensor memory
-//                  for the whole CTA (so no atomics for them), and the CTA walks
+//                  for the whole item (so no atomics for them), and the CTA walks
 //                  every query tile that can see a key of tile j (causal: rows
 //                  at positions i + kv_offset >= the tile's first key, with
-//                  kv_offset = Skv - Sq) of every query head of the group.
+//                  kv_offset = Skv - Sq) of every query head of the group. An
+//                  item's dK, dV write-out overlaps the next item's K, V loads
+//                  and first products.
 //                  Per step, on the tensor cores:
 //                    S^T  = K_j Q_i^T          -> TMEM (kv rows x q cols)
 //                    dP^T = V_j dO_i^T         -> TMEM
@@ -28,7 +33,7 @@
 //                                                 shared memory
 //   3. dq_convert: dq = scale * accumulator, rounded to the input type.
 //
-// Warp roles of bwd_main (320 threads): warp 0 TMA producer (K_j, V_j once;
+// Warp roles of bwd_main (320 threads): warp 0 TMA producer (K_j, V_j once per item;
 // Q_i with L_i, D_i through a 2-slot ring, dO_i through one slot at d = 128;
 // three slots each at d = 64), warp 1 MMA issuer and TMEM
 // owner, warps 2-9 compute P^T and dS^T (one thread per key row, two warps per
@@ -71,9 +76,9 @@ struct BwdCfg {
   static constexpr int kOffDqS = kOffDS + kDsBytes;                // [8 warps] (d = 128)
   static constexpr int kOffRow = kOffDqS + 8 * kDqStageBytes;     // [kQStages] x (L2 | D) x 128 f32
   static constexpr int kOffBar = kOffRow + kQStages * 1024;
-  // kv_full, q_full[NQ], q_empty[NQ], do_full[ND], do_empty[ND], s_full,
+  // kv_full, kv_empty, q_full[NQ], q_empty[NQ], do_full[ND], do_empty[ND], s_full,
   // dp_full, p_full, ds_full, dv_done, dq_full, dq_empty, ds_empty, kd_done, drain
-  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDoStages + 10;
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 10;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
 };
@@ -147,6 +152,7 @@ __global__ void __launch_bounds__(256, 8) bwd_pre_kernel(const BwdPreParams p) {
       for (int e = u; e < p.d / 4; e += U) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+  if (p.work && blockIdx.x == 0 && threadIdx.x == 0) *p.work = 0;
 }
 
 // -------------------------------------------------------------- convert --
@@ -176,6 +182,29 @@ __global__ void __launch_bounds__(256, 8) dq_convert_kernel(const DqConvertParam
 }
 
 // ----------------------------------------------------------------- main --
+// A work item is one key tile j of one (batch, key/value head): item
+// w = j * B * Hkv + (b * Hkv + g), so that low j (most query tiles under the
+// causal mask) comes first.
+struct BwdItem {
+  int j, bkv, b, g;
+  int i_start, n_i, n_iter;
+};
+
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int w) {
+  BwdItem it;
+  const int BHkv = p.B * p.Hkv;
+  it.j = w / BHkv;
+  it.bkv = w % BHkv;
+  it.b = it.bkv / p.Hkv;
+  it.g = it.bkv % p.Hkv;
+  // causal: the first query tile holding a row at position >= this tile's
+  // first key (query row i stands at position i + kv_offset)
+  it.i_start = p.causal ? max(0, it.j * kTileN - p.kv_offset) / kTileM : 0;
+  it.n_i = p.n_q_tiles - it.i_start;
+  it.n_iter = (p.Hq / p.Hkv) * it.n_i;
+  return it;
+}
+
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
@@ -195,14 +224,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  // the work item whose K_j, V_j the current kv_full phase delivers
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
   const uint32_t bar0 = sbase + Cfg::kOffBar;
   const uint32_t kv_full = bar0;
-  auto q_full = [&](int s) { return bar0 + 8 * (1 + s); };
-  auto q_empty = [&](int s) { return bar0 + 8 * (1 + NQ + s); };
-  auto do_full = [&](int s) { return bar0 + 8 * (1 + 2 * NQ + s); };
-  auto do_empty = [&](int s) { return bar0 + 8 * (1 + 2 * NQ + ND + s); };
-  const uint32_t s_full = bar0 + 8 * (1 + 2 * NQ + 2 * ND);
+  const uint32_t kv_empty = bar0 + 8;
+  auto q_full = [&](int s) { return bar0 + 8 * (2 + s); };
+  auto q_empty = [&](int s) { return bar0 + 8 * (2 + NQ + s); };
+  auto do_full = [&](int s) { return bar0 + 8 * (2 + 2 * NQ + s); };
+  auto do_empty = [&](int s) { return bar0 + 8 * (2 + 2 * NQ + ND + s); };
+  const uint32_t s_full = bar0 + 8 * (2 + 2 * NQ + 2 * ND);
   const uint32_t dp_full = s_full + 8;
   const uint32_t p_full = s_full + 16;
   const uint32_t ds_full = s_full + 24;
@@ -215,24 +247,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
-
-  // ---- work: key tile j of (batch, kv head); small j first (most query tiles) ----
-  const int BHkv = p.B * p.Hkv;
-  const int j = static_cast<int>(blockIdx.x) / BHkv;
-  const int bkv = static_cast<int>(blockIdx.x) % BHkv;
-  const int b = bkv / p.Hkv, g = bkv % p.Hkv;
-  const int G = p.Hq / p.Hkv;
-  const int n_qt = p.n_q_tiles;                  // query tiles per head
-  // causal: the first query tile holding a row at position >= this tile's
-  // first key (query row i stands at position i + kv_offset)
-  const int i_start = p.causal ? max(0, j * kTileN - p.kv_offset) / kTileM : 0;
-  const int n_i = n_qt - i_start;
-  const int n_iter = G * n_i;
-  auto bh_of = [&](int it) { return b * p.Hq + g * G + it / n_i; };
-  auto i_of = [&](int it) { return i_start + it % n_i; };
+  const int n_items = p.n_kv_tiles * p.B * p.Hkv;
+  if (threadIdx.x == 0) {
+    trace_span(p.trace, 0, clock64());
+    trace_span(p.trace, 1, smid());
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
     for (int s = 0; s < NQ; ++s) {
       mbar_init(q_full(s), 1);
       mbar_init(q_empty(s), 1 + 8);   // MMA commit + one per compute warp (L, D rows)
@@ -263,31 +286,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // launched as the pre-pass's programmatic dependent: everything above ran
-  // alongside it; the D, L and zeroed dQ rows it writes are read below
+  // alongside it; the D, L, zeroed dQ rows and the zeroed item counter it
+  // writes are read below
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  // Steps (one query tile of one query head against the item's key tile) are
+  // counted across the CTA's items, so every ring slot and barrier phase
+  // below follows a global step count.
   if (warp == 0) {
     // ===================== TMA producer =====================
+    // Claims items from the launch's counter. The next item's first Q and dO
+    // go out as soon as their ring slots free, then its K_j, V_j once the
+    // current item's last products have read K and V (kv_empty); the item
+    // index is published with the kv_full arrival (an index past the last
+    // item, with no bytes, ends the consumers' loops).
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTileBytes);
-      for (int c = 0; c < Cfg::kChunks; ++c) {
-        tma_load_3d(sbase + Cfg::kOffK + c * (kTileN * 128), &p.tm_k, kv_full, c * kChunk,
-                    j * kTileN, bkv);
-        tma_load_3d(sbase + Cfg::kOffV + c * (kTileN * 128), &p.tm_v, kv_full, c * kChunk,
-                    j * kTileN, bkv);
-      }
+      tma_prefetch_desc(&p.tm_dk);
+      tma_prefetch_desc(&p.tm_dv);
       Tracer tr(p.trace, 0);
       int nq = 0, ndo = 0;   // Q and dO tiles issued
-      for (int it = 0; it < n_iter; ++it) {
-        const int bh = bh_of(it), i = i_of(it);
-        const int sq = it % NQ;
-        if (it >= NQ &&
-            !mbar_wait(q_empty(sq), static_cast<uint32_t>(it / NQ - 1) & 1, abort_flag, p.status))
-          break;
+      int kv_pending = -1;   // kv_full phase whose K, V loads may be in flight
+      bool ok = true;
+      // one step's Q (with its L, D rows) and dO
+      auto load_step = [&](const BwdItem& I, int s) -> bool {
+        const int bh = I.b * p.Hq + I.g * (p.Hq / p.Hkv) + s / I.n_i;
+        const int i = I.i_start + s % I.n_i;
+        const int sq = nq % NQ;
+        if (nq >= NQ &&
+            !mbar_wait(q_empty(sq), static_cast<uint32_t>(nq / NQ - 1) & 1, abort_flag, p.status))
+          return false;
         tr(41);
         const uint32_t fq = q_full(sq);
         mbar_arrive_expect_tx(fq, Cfg::kTileBytes + 1024);
@@ -298,10 +329,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bulk_load(sbase + Cfg::kOffRow + sq * 1024, p.lse2 + roff, 512, fq);
         bulk_load(sbase + Cfg::kOffRow + sq * 1024 + 512, p.delta + roff, 512, fq);
         ++nq;
-        const int sd = it % ND;
-        if (it >= ND &&
-            !mbar_wait(do_empty(sd), static_cast<uint32_t>(it / ND - 1) & 1, abort_flag, p.status))
-          break;
+        const int sd = ndo % ND;
+        if (ndo >= ND &&
+            !mbar_wait(do_empty(sd), static_cast<uint32_t>(ndo / ND - 1) & 1, abort_flag, p.status))
+          return false;
         const uint32_t fd = do_full(sd);
         mbar_arrive_expect_tx(fd, Cfg::kTileBytes);
         for (int c = 0; c < Cfg::kChunks; ++c)
@@ -309,9 +340,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       fd, c * kChunk, i * kTileM, bh);
         ++ndo;
         tr(40);
+        return true;
+      };
+      int w = atomicAdd(p.work, 1);
+      for (int k = 0; ok; ++k) {
+        BwdItem I{};
+        if (w < n_items) {
+          I = bwd_item(p, w);
+          if (!(ok = load_step(I, 0))) break;
+        }
+        if (k > 0) {
+          if (!(ok = mbar_wait(kv_empty, (k - 1) & 1, abort_flag, p.status))) break;
+          kv_pending = -1;
+        }
+        tr(95);
+        *item_slot = w;
+        if (w >= n_items) {
+          mbar_arrive(kv_full);
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full, 2 * Cfg::kTileBytes);
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+          tma_load_3d(sbase + Cfg::kOffK + c * (kTileN * 128), &p.tm_k, kv_full, c * kChunk,
+                      I.j * kTileN, I.bkv);
+          tma_load_3d(sbase + Cfg::kOffV + c * (kTileN * 128), &p.tm_v, kv_full, c * kChunk,
+                      I.j * kTileN, I.bkv);
+        }
+        kv_pending = k;
+        for (int s = 1; ok && s < I.n_iter; ++s) ok = load_step(I, s);
+        if (!ok) break;
+        w = atomicAdd(p.work, 1);
+        if (w < n_items) {   // the next item's K_j, V_j into L2 while this item runs
+          const BwdItem J = bwd_item(p, w);
+          for (int c = 0; c < Cfg::kChunks; ++c) {
+            tma_prefetch_l2_3d(&p.tm_k, c * kChunk, J.j * kTileN, J.bkv);
+            tma_prefetch_l2_3d(&p.tm_v, c * kChunk, J.j * kTileN, J.bkv);
+          }
+        }
       }
       if (*abort_flag) {
-        drain_wait(kv_full, 0, p.status);
+        if (kv_pending >= 0) drain_wait(kv_full, static_cast<uint32_t>(kv_pending) & 1, p.status);
         for (int jj = max(0, nq - NQ); jj < nq; ++jj)
           drain_wait(q_full(jj % NQ), static_cast<uint32_t>(jj / NQ) & 1, p.status);
         for (int jj = max(0, ndo - ND); jj < ndo; ++jj)
@@ -324,6 +392,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // follow soon after dS(n); S^T(n+1) as soon as dV(n) has read P^T(n)):
     //   dV(n) [P(n) ready]  dQ(n) [dS(n) ready]  S^T(n+1) [dV(n) done]
     //   dK(n)  dP^T(n+1) [dQ(n) read out of TMEM]
+    // After an item's last step: kv_empty (K, V read for the last time by
+    // that dQ), dK, kd_done; the next item's S^T and dP^T once its K, V land.
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kTileM, kBf16, false, false);  // S^T, dP^T
       constexpr uint32_t idesc_kv = make_idesc(128, D, kBf16, false, true);       // dV, dK
@@ -357,80 +427,89 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto do_desc_mn = [&](int s) { return do_desc0_mn + s * kSlot; };
       constexpr int kCB = kTileN * 128;   // bytes of one 64-column chunk of a 128-row tile
 
-      auto issue_s = [&](int st) {   // S^T = K_j Q_i^T, both K-major
-        mma_ss_product<D / 16, true, kCB, true, kCB>(t_s, k_desc, q_desc(st), idesc_s, 0);
+      Tracer tr(p.trace, 1);
+      // S^T(g) = K_j Q_i^T once Q_i has landed and dV(g-1) has read P^T(g-1)
+      auto issue_s = [&](int g) -> bool {
+        if (!mbar_wait(q_full(g % NQ), static_cast<uint32_t>(g / NQ) & 1, abort_flag, p.status))
+          return false;
+        if (g > 0 && !mbar_wait(dv_done, (g - 1) & 1, abort_flag, p.status)) return false;
+        tr(5);
+        tc_fence_after();
+        mma_ss_product<D / 16, true, kCB, true, kCB>(t_s, k_desc, q_desc(g % NQ), idesc_s, 0);
         tc_commit(s_full);
+        return true;
       };
-      auto issue_dp = [&](int st) {   // dP^T = V_j dO_i^T, both K-major
-        mma_ss_product<D / 16, true, kCB, true, kCB>(t_dp, v_desc, do_desc(st), idesc_s, 0);
+      // dP^T(g) = V_j dO_i^T once dO_i has landed and dQ(g-1) has left TMEM
+      auto issue_dp = [&](int g) -> bool {
+        if (g > 0 && !mbar_wait(dq_empty, (g - 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(do_full(g % ND), static_cast<uint32_t>(g / ND) & 1, abort_flag, p.status))
+          return false;
+        tr(7);
+        tc_fence_after();
+        mma_ss_product<D / 16, true, kCB, true, kCB>(t_dp, v_desc, do_desc(g % ND), idesc_s, 0);
         tc_commit(dp_full);
+        return true;
       };
 
-      Tracer tr(p.trace, 1);
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status) &&
-                mbar_wait(q_full(0), 0, abort_flag, p.status) &&
-                mbar_wait(do_full(0), 0, abort_flag, p.status);
+      bool ok = true;
+      int g = 0;   // global step
+      for (int k = 0; ok; ++k) {
+        if (!(ok = mbar_wait(kv_full, k & 1, abort_flag, p.status))) break;
+        tr(91);
+        const int w = *item_slot;
+        if (w >= n_items) break;
 #ifdef FA_WAIT_TEST
-      // wait-limit test build: nothing completes this phase before the abort
-      // path's own commit, so the wait runs out
-      if (ok) ok = mbar_wait(drain, 0, abort_flag, p.status);
+        // wait-limit test build: nothing completes this phase before the abort
+        // path's own commit, so the wait runs out
+        if (k == 0 && !(ok = mbar_wait(drain, 0, abort_flag, p.status))) break;
 #endif
-      tr(9);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-      }
-      for (int n = 0; ok && n < n_iter; ++n) {
-        const int st = n % NQ;
-        const int st1 = (n + 1) % NQ;
-        const int sd = n % ND;
-        const int sd1 = (n + 1) % ND;
-        const bool more = n + 1 < n_iter;
-        // dV += P^T dO_i  (P^T from TMEM, 16-bit packed: query columns 0-63 in
-        // S^T's columns 0-31, columns 64-127 in S^T's columns 96-127)
-        if (!(ok = mbar_wait(p_full, n & 1, abort_flag, p.status))) break;
-        tr(1);
-        tc_fence_after();
-        mma_ts_product8<false, 0, 64>(t_dv, t_s, do_desc_mn(sd), idesc_kv, n > 0 ? 1u : 0u);
-        tc_commit(dv_done);
-        tc_commit(do_empty(sd));
-        // dQ (into dP^T's columns: the compute warps have read dP^T(n))
-        if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, p.status))) break;
-        tr(3);
-        tc_fence_after();
-        // dQ = dS K_j, both operands MN-major
-        mma_ss_product<kTileN / 16, false, 0, false, 0>(t_dp, ds_desc_mn, k_desc_mn, idesc_q, 0);
-        tc_commit(dq_full);
-        // S^T for the next step, once dV(n) has consumed P^T(n)
-        if (more) {
-          if (!(ok = mbar_wait(q_full(st1), static_cast<uint32_t>((n + 1) / NQ) & 1,
-                               abort_flag, p.status)))
-            break;
-          if (!(ok = mbar_wait(dv_done, n & 1, abort_flag, p.status))) break;
-          tr(5);
+        tr(9);
+        const int N = bwd_item(p, w).n_iter;
+        if (!(ok = issue_s(g) && issue_dp(g))) break;
+        for (int n = 0; n < N; ++n, ++g) {
+          const int st = g % NQ;
+          const int sd = g % ND;
+          const bool more = n + 1 < N;
+          // dV += P^T dO_i  (P^T from TMEM, 16-bit packed: query columns 0-63 in
+          // S^T's columns 0-31, columns 64-127 in S^T's columns 96-127)
+          if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
+          tr(1);
           tc_fence_after();
-          issue_s(st1);
-        }
-        // dK += dS^T Q_i; then dS^T and stage st (Q_i, dO_i) are free
-        mma_ss_product<kTileM / 16, true, kCB, false, 0>(t_dk, ds_desc, q_desc_mn(st), idesc_kv,
-                                                        n > 0 ? 1u : 0u);
-        tc_commit(ds_empty);
-        tc_commit(q_empty(st));
-        tr(6);
-        // dP^T for the next step, once dQ(n) has left TMEM
-        if (more) {
-          if (!(ok = mbar_wait(dq_empty, n & 1, abort_flag, p.status))) break;
-          if (!(ok = mbar_wait(do_full(sd1), static_cast<uint32_t>((n + 1) / ND) & 1, abort_flag,
-                               p.status)))
-            break;
-          tr(7);
+          mma_ts_product8<false, 0, 64>(t_dv, t_s, do_desc_mn(sd), idesc_kv, n > 0 ? 1u : 0u);
+          tc_commit(dv_done);
+          tc_commit(do_empty(sd));
+          // dQ (into dP^T's columns: the compute warps have read dP^T(n))
+          if (!(ok = mbar_wait(ds_full, g & 1, abort_flag, p.status))) break;
+          tr(3);
           tc_fence_after();
-          issue_dp(sd1);
+          // dQ = dS K_j, both operands MN-major
+          mma_ss_product<kTileN / 16, false, 0, false, 0>(t_dp, ds_desc_mn, k_desc_mn, idesc_q, 0);
+          tc_commit(dq_full);
+          // S^T for the next step of this item; after its last step K and V
+          // are free for the next item's
+          if (more) {
+            if (!(ok = issue_s(g + 1))) break;
+          } else {
+            tc_commit(kv_empty);
+          }
+          // dK += dS^T Q_i; then dS^T and stage st (Q_i, dO_i) are free
+          mma_ss_product<kTileM / 16, true, kCB, false, 0>(t_dk, ds_desc, q_desc_mn(st), idesc_kv,
+                                                          n > 0 ? 1u : 0u);
+          tc_commit(ds_empty);
+          tc_commit(q_empty(st));
+          tr(6);
+          // dP^T for the next step, once dQ(n) has left TMEM
+          if (more && !(ok = issue_dp(g + 1))) break;
         }
+        if (!ok) break;
+        tc_commit(kd_done);   // dK, dV of this item are complete in TMEM
+        tr(90);
       }
-      tc_commit(ok ? kd_done : drain);
-      if (!ok) drain_wait(drain, 0, p.status);
+      trace_span(p.trace, 5, clock64());
+      if (!ok) {
+        tc_commit(drain);
+        drain_wait(drain, 0, p.status);
+      }
     }
   } else {
     // ============ P^T, dS^T and the dQ read-out (warps 2-9) ============
@@ -443,7 +522,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = (warp - 2) >> 2;
     const int c0 = half * 64;                   // first query column of this warp
     const int r = quarter * 32 + lane;
-    const int kv = j * kTileN + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + 256;
     const uint32_t t_dp = tmem + lane_off + 384;
@@ -480,156 +558,194 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bulk_commit_group();
       }
     };
-    for (int it = 0; it < n_iter; ++it) {
-      const int st = it % NQ;
-      const uint32_t par = static_cast<uint32_t>(it / NQ) & 1;
-      const int i = i_of(it);
-      const float* rowv = reinterpret_cast<const float*>(smem + Cfg::kOffRow + st * 1024);
-      const float* l2s = rowv + c0;          // L * log2(e) per query column
-      const float* dls = rowv + 128 + c0;    // D per query column
-      ok = __all_sync(0xffffffffu, mbar_wait(q_full(st), par, abort_flag, p.status));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, p.status));
+    int g = 0;   // global step
+    for (int k = 0; ok; ++k) {
+      ok = __all_sync(0xffffffffu, mbar_wait(kv_full, k & 1, abort_flag, p.status));
       if (!ok) break;
-      tr(20);
-      tc_fence_after();
-      // Masked entries: key past the sequence end, or (causal) key after the
-      // query's position q + kv_offset. Column e of this warp's half is masked
-      // iff e < thr; thr <= 0 on every tile that is neither diagonal nor
-      // ragged, which skip the selects.
-      const int q0 = i * kTileM + c0;
-      const int thr = kv >= p.Skv ? 64 : (p.causal ? min(kv - p.kv_offset - q0, 64) : 0);
-      const bool any_mask = __any_sync(0xffffffffu, thr > 0);
-      uint32_t ppk[32];
-      {
-        uint32_t raw[64];
-        tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
-        tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
-        tmem_wait_ld();
-        if (any_mask) {
+      const int w = *item_slot;
+      if (w >= n_items) break;
+      const BwdItem I = bwd_item(p, w);
+      const int kv = I.j * kTileN + r;
+      for (int it = 0; it < I.n_iter; ++it, ++g) {
+        const int st = g % NQ;
+        const uint32_t par = static_cast<uint32_t>(g / NQ) & 1;
+        const int i = I.i_start + it % I.n_i;
+        const float* rowv = reinterpret_cast<const float*>(smem + Cfg::kOffRow + st * 1024);
+        const float* l2s = rowv + c0;          // L * log2(e) per query column
+        const float* dls = rowv + 128 + c0;    // D per query column
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full(st), par, abort_flag, p.status));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort_flag, p.status));
+        if (!ok) break;
+        tr(20);
+        if (g == 0 && warp == 2 && lane == 0) trace_span(p.trace, 3, clock64());
+        tc_fence_after();
+        // Masked entries: key past the sequence end, or (causal) key after the
+        // query's position q + kv_offset. Column e of this warp's half is masked
+        // iff e < thr; thr <= 0 on every tile that is neither diagonal nor
+        // ragged, which skip the selects.
+        const int q0 = i * kTileM + c0;
+        const int thr = kv >= p.Skv ? 64 : (p.causal ? min(kv - p.kv_offset - q0, 64) : 0);
+        const bool any_mask = __any_sync(0xffffffffu, thr > 0);
+        uint32_t ppk[32];
+        {
+          uint32_t raw[64];
+          tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
+          tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+          tmem_wait_ld();
+          if (any_mask) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) raw[e] = (e < thr) ? __float_as_uint(-INFINITY) : raw[e];
-        }
-        const uint64_t c2 = f2_pack(c, c);
+            for (int e = 0; e < 64; ++e) raw[e] = (e < thr) ? __float_as_uint(-INFINITY) : raw[e];
+          }
+          const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float2 l2 = *reinterpret_cast<const float2*>(l2s + e);
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), c2,
-                           f2_pack(-l2.x, -l2.y)), x0, x1);
-          ppk[e / 2] = pack2<kBf16>(ex2(x0), ex2(x1));
+          for (int e = 0; e < 64; e += 2) {
+            const float2 l2 = *reinterpret_cast<const float2*>(l2s + e);
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])), c2,
+                             f2_pack(-l2.x, -l2.y)), x0, x1);
+            ppk[e / 2] = pack2<kBf16>(ex2(x0), ex2(x1));
+          }
+          tmem_st32(t_s + half * 96, ppk);
         }
-        tmem_st32(t_s + half * 96, ppk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-      tr(21);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        tr(21);
 
-      if (it > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (it - 1) & 1, abort_flag, p.status));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, it & 1, abort_flag, p.status));
+        if (g > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (g - 1) & 1, abort_flag, p.status));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, abort_flag, p.status));
+        if (!ok) break;
+        tr(22);
+        tc_fence_after();
+        {
+          uint32_t raw[64];
+          tmem_ld32(t_dp + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
+          tmem_ld32(t_dp + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+          tmem_wait_ld();
+          uint32_t wv[32];
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float2 pp = unpack2<kBf16>(ppk[e / 2]);
+            const float2 dd = *reinterpret_cast<const float2*>(dls + e);
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(pp.x, pp.y),
+                             f2_sub(f2_pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])),
+                                    f2_pack(dd.x, dd.y))), d0, d1);
+            wv[e / 2] = pack2<kBf16>(d0, d1);
+          }
+          // the previous item's dK or dV store reads these rows (below)
+          if (it == 0) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+          // this warp's 64 query columns = one 128-byte row of chunk `half`;
+          // 16-byte unit u of row r sits at unit u ^ (r % 8) (128-byte swizzle)
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
+                make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(ds_full);
+          mbar_arrive(q_empty(st));
+        }
+        tr(23);
+        if constexpr (D == 128) {
+          if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
+          pend_x = -1;
+          tr(34);
+        }
+
+        // dQ(it): TMEM -> fp32 accumulator. This thread holds head-dimension
+        // entries [half * D/2, (half + 1) * D/2) of query row r of the tile.
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, p.status));
+        if (!ok) break;
+        tr(30);
+        tc_fence_after();
+        constexpr int kCols = D / 2;
+        uint32_t acc[kCols];
+#pragma unroll
+        for (int cc = 0; cc < kCols / 32; ++cc)
+          tmem_ld32(t_dp + half * kCols + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_empty);
+        tr(31);
+        const int bh = I.b * p.Hq + I.g * (p.Hq / p.Hkv) + it / I.n_i;
+        if constexpr (D == 128) {
+          reduce_box(acc, half * 64, i * kTileM + quarter * 32, bh);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
+          pend_x = half * 64 + 32;
+          pend_y = i * kTileM + quarter * 32;
+          pend_bh = bh;
+        } else {   // d = 64: the step's 32 columns are one box
+          reduce_box(acc, half * 32, i * kTileM + quarter * 32, bh);
+        }
+        tr(32);
+      }
       if (!ok) break;
-      tr(22);
+      if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
+      pend_x = -1;
+      // ---- epilogue: warps 2-5 write dK = scale * accumulated dS^T Q, warps 6-9 dV ----
+      // (the next item's first dV and dK, which overwrite these columns, wait
+      // for this CTA's compute warps' P^T arrivals, which follow this read-out)
+      // This warp's 32 key rows go out as 128-byte-swizzled boxes of 32 rows x
+      // 64 columns through bulk tensor stores (rows past Skv are not written):
+      // columns 0-63 staged over its own dS^T rows (free: every product of the
+      // item is complete), columns 64-127 (d = 128) in its dQ staging box.
+      ok = __all_sync(0xffffffffu, mbar_wait(kd_done, k & 1, abort_flag, p.status));
+      if (!ok) break;
+      tr(93);
       tc_fence_after();
       {
-        uint32_t raw[64];
-        tmem_ld32(t_dp + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
-        tmem_ld32(t_dp + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
-        tmem_wait_ld();
-        uint32_t w[32];
+        const float f = half == 0 ? p.scale : 1.f;
+        const uint32_t box0 = sbase + Cfg::kOffDS + half * (kTileN * 128) + quarter * 32 * 128;
+        if (lane == 0) bulk_wait_read_all();   // the dQ box's last reduce has read it
+        __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float2 pp = unpack2<kBf16>(ppk[e / 2]);
-          const float2 dd = *reinterpret_cast<const float2*>(dls + e);
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(pp.x, pp.y),
-                           f2_sub(f2_pack(__uint_as_float(raw[e]), __uint_as_float(raw[e + 1])),
-                                  f2_pack(dd.x, dd.y))), d0, d1);
-          w[e / 2] = pack2<kBf16>(d0, d1);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + half * 128 + cc * 32, o);
+          tmem_wait_ld();
+          const uint32_t row = (cc < 2 ? box0 : dq_stage) + lane * 128;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + v);   // 16-byte unit of the row
+            st_shared_v4(row + ((u ^ (lane & 7)) << 4),
+                         pack2<kBf16>(__uint_as_float(o[8 * v]) * f, __uint_as_float(o[8 * v + 1]) * f),
+                         pack2<kBf16>(__uint_as_float(o[8 * v + 2]) * f, __uint_as_float(o[8 * v + 3]) * f),
+                         pack2<kBf16>(__uint_as_float(o[8 * v + 4]) * f, __uint_as_float(o[8 * v + 5]) * f),
+                         pack2<kBf16>(__uint_as_float(o[8 * v + 6]) * f, __uint_as_float(o[8 * v + 7]) * f));
+          }
         }
-        // this warp's 64 query columns = one 128-byte row of chunk `half`;
-        // 16-byte unit u of row r sits at unit u ^ (r % 8) (128-byte swizzle)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
-              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int y = I.j * kTileN + quarter * 32;
+        if (lane == 0 && y < p.Skv) {
+          const CUtensorMap* tm = half == 0 ? &p.tm_dk : &p.tm_dv;
+          tma_store_3d(tm, box0, 0, y, I.bkv);
+          if constexpr (D == 128) tma_store_3d(tm, dq_stage, kChunk, y, I.bkv);
+          bulk_commit_group();
+        }
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(ds_full);
-        mbar_arrive(q_empty(st));
-      }
-      tr(23);
-      if constexpr (D == 128) {
-        if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
-        pend_x = -1;
-        tr(34);
-      }
-
-      // dQ(it): TMEM -> fp32 accumulator. This thread holds head-dimension
-      // entries [half * D/2, (half + 1) * D/2) of query row r of the tile.
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.status));
-      if (!ok) break;
-      tr(30);
-      tc_fence_after();
-      constexpr int kCols = D / 2;
-      uint32_t acc[kCols];
-#pragma unroll
-      for (int cc = 0; cc < kCols / 32; ++cc)
-        tmem_ld32(t_dp + half * kCols + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
-      tr(31);
-      const int bh = bh_of(it);
-      if constexpr (D == 128) {
-        reduce_box(acc, half * 64, i * kTileM + quarter * 32, bh);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
-        pend_x = half * 64 + 32;
-        pend_y = i * kTileM + quarter * 32;
-        pend_bh = bh;
-      } else {   // d = 64: the step's 32 columns are one box
-        reduce_box(acc, half * 32, i * kTileM + quarter * 32, bh);
-      }
-      tr(32);
+      tr(94);
     }
-    if (ok && pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
     // the bulk reduces read this warp's staging box until they complete
     if (lane == 0) bulk_wait_all();
     __syncwarp();
-    // ---- epilogue: warps 2-5 write dK = scale * accumulated dS^T Q, warps 6-9 dV ----
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(kd_done, 0, abort_flag, p.status));
-    if (ok) {
-      tc_fence_after();
-      using Elem = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      const float f = half == 0 ? p.scale : 1.f;
-      Elem* dst = reinterpret_cast<Elem*>(half == 0 ? p.dk : p.dv) +
-                  (static_cast<size_t>(bkv) * p.Skv + kv) * D;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + half * 128 + cc * 32, o);
-        tmem_wait_ld();
-        if (kv < p.Skv) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            d4[v] = make_uint4(
-                pack2<kBf16>(__uint_as_float(o[8 * v]) * f, __uint_as_float(o[8 * v + 1]) * f),
-                pack2<kBf16>(__uint_as_float(o[8 * v + 2]) * f, __uint_as_float(o[8 * v + 3]) * f),
-                pack2<kBf16>(__uint_as_float(o[8 * v + 4]) * f, __uint_as_float(o[8 * v + 5]) * f),
-                pack2<kBf16>(__uint_as_float(o[8 * v + 6]) * f, __uint_as_float(o[8 * v + 7]) * f));
-        }
-      }
-    }
+    if (warp == 2 && lane == 0) trace_span(p.trace, 4, clock64());
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_span(p.trace, 6, clock64());
   // the dQ convert kernel (this grid's programmatic dependent) may be
   // scheduled once every CTA got here; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -664,7 +780,14 @@ cudaError_t launch_bwd_impl(const BwdParams& p, cudaStream_t stream) {
   auto kernel = fa_bwd_kernel<D, kBf16>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.n_kv_tiles * p.B * p.Hkv);
+  // persistent: one CTA per SM (the shared and tensor memory of one CTA fill
+  // an SM), fewer when there are fewer items
+  int dev = 0, n_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long n_items = static_cast<long long>(p.n_kv_tiles) * p.B * p.Hkv;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(n_items, std::max(n_sm, 1)));
   e = launch_dependent(kernel, dim3(grid), dim3(kBwdThreads), smem, stream, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

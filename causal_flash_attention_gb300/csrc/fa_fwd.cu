@@ -137,6 +137,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     else n_t[t] = p.causal ? min(q0 / kTileN + p.kv_tiles_ahead, n_kv_total) : n_kv_total;
   }
   const int n_load = max(n_t[0], n_t[1]);
+  if (threadIdx.x == 0) {
+    trace_span(p.trace, 0, clock64());
+    trace_span(p.trace, 1, smid());
+    trace_span(p.trace, 2, n_t[0] + n_t[1]);
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full, 1);
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bars.sf(t), j & 1, abort_flag, p.status));
       if (!ok) break;
       tr(60);
+      if (j == 0 && warp == 2 && lane == 0) trace_span(p.trace, 3, clock64());
       tc_fence_after();
       float s[kTileN];
       {
@@ -377,6 +383,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (n - 1) & 1, abort_flag, p.status));
+      if (warp == 2 && lane == 0) trace_span(p.trace, 4, clock64());
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.f / l;
@@ -407,6 +414,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_span(p.trace, 6, clock64());
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

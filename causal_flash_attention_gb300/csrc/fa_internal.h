@@ -44,6 +44,7 @@ struct BwdPreParams {
   float* delta;       // [B*Hq][Sq_pad]   D_i = <dO_i, O_i>, 0 on padding rows
   float* lse2;        // [B*Hq][Sq_pad]   LSE_i * log2(e), +inf on padding rows
   float* dq_acc;      // [B*Hq][Sq_pad][d] fp32, zeroed here
+  int* work;          // the main kernel's work-item counter, zeroed here (null: none)
   int BH, Sq, Sq_pad, d;
   int dtype;
 };
@@ -54,16 +55,19 @@ struct BwdParams {
   CUtensorMap tm_v;   // [B*Hkv][Skv][d]
   CUtensorMap tm_do;  // [B*Hq][Sq][d]
   CUtensorMap tm_dq;  // dq_acc as fp32 [B*Hq][Sq_pad][d], box (32, 32, 1), 128B swizzle
+  CUtensorMap tm_dk;  // dk [B*Hkv][Skv][d], box (64, 32, 1), 128B swizzle (stores)
+  CUtensorMap tm_dv;  // dv, as tm_dk
   const float* delta; // [B*Hq][Sq_pad]
   const float* lse2;  // [B*Hq][Sq_pad]
   float* dq_acc;      // [B*Hq][Sq_pad][d]
   void* dk;           // [B*Hkv][Skv][d]
   void* dv;           // [B*Hkv][Skv][d]
+  int* work;          // work-item counter, zeroed by the pre-pass
   int B, Hq, Hkv, Sq, Skv, Sq_pad, kv_offset;
   int causal;
   float scale;        // softmax scale
   float scale_log2;   // softmax scale * log2(e)
-  int n_kv_tiles;     // ceil(Skv / 128): CTAs per (batch, key/value head)
+  int n_kv_tiles;     // ceil(Skv / 128): work items per (batch, key/value head)
   int n_q_tiles;      // ceil(Sq / 128)
   int* status;
   unsigned long long* trace;   // timeline buffer of trace builds (FA_TRACE); else null

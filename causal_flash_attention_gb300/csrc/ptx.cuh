@@ -54,11 +54,27 @@ struct Tracer {
       base[n++] = (static_cast<unsigned long long>(clock64()) << 8) | static_cast<unsigned>(ev);
   }
 };
+// Every CTA of a launch (up to kTraceSpanCtas) also fills kTraceSpanSlots
+// entries after the timeline region: its SM, its work count and clock64
+// readings at points the kernel chooses (start, first step, last step, end).
+constexpr int kTraceSpanCtas = 16384, kTraceSpanSlots = 8;
+__device__ __forceinline__ void trace_span(unsigned long long* buf, int slot, unsigned long long v) {
+  if (buf && blockIdx.x < kTraceSpanCtas)
+    buf[static_cast<size_t>(kTraceCtas) * kTraceRoles * kTraceSlots +
+        static_cast<size_t>(blockIdx.x) * kTraceSpanSlots + slot] = v;
+}
+__device__ __forceinline__ unsigned smid() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
 #else
 struct Tracer {
   __device__ Tracer(unsigned long long*, int) {}
   __device__ void operator()(int) {}
 };
+__device__ __forceinline__ void trace_span(unsigned long long*, int, unsigned long long) {}
+__device__ __forceinline__ unsigned smid() { return 0; }
 #endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -167,6 +183,25 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 3-D tiled store of one box from shared memory; completion through the
+// bulk group (rows past the tensor's extent are not written).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Prefetch one box of a tiled tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

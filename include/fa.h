@@ -95,7 +95,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
  * Bytes of device workspace fa_bwd needs for these sizes (the same for every
  * dtype): an fp32 dQ accumulator [B][Hq][S128][d], D and LSE*log2(e) rows
  * [B][Hq][S128] each, where S128 = S rounded up to a multiple of 128, each
- * region starting on a 256-byte boundary. Returns 0 for invalid sizes.
+ * region starting on a 256-byte boundary, then 256 bytes holding the
+ * counter from which the main kernel's CTAs claim work items. Returns 0 for
+ * invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int S, int d);
 

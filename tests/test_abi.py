@@ -89,7 +89,7 @@ def test_workspace_size_formula(fa_lib):
     def expect(B, Hq, S, d):
         up = lambda x, m: (x + m - 1) // m * m
         bh, sp = B * Hq, up(S, 128)
-        return up(bh * sp * d * 4, 256) + 2 * up(bh * sp * 4, 256)
+        return up(bh * sp * d * 4, 256) + 2 * up(bh * sp * 4, 256) + 256
     for B, Hq, Hkv, S, d in [(1, 2, 2, 128, 64), (8, 12, 12, 1024, 64), (4, 32, 8, 2048, 128),
                              (1, 32, 32, 8192, 128), (1, 1, 1, 1, 64), (3, 4, 2, 200, 128)]:
         assert fa_lib.fa_bwd_workspace_bytes(B, Hq, Hkv, S, d) == expect(B, Hq, S, d)
@@ -151,7 +151,7 @@ def test_kv_workspace_is_sized_by_the_query_length(fa_lib):
     for B, Hq, Hkv, Sq, Skv, d in [(1, 32, 8, 2048, 8192, 128), (2, 4, 2, 1, 777, 64),
                                    (1, 2, 2, 300, 129, 128)]:
         bh, sp = B * Hq, up(Sq, 128)
-        want = up(bh * sp * d * 4, 256) + 2 * up(bh * sp * 4, 256)
+        want = up(bh * sp * d * 4, 256) + 2 * up(bh * sp * 4, 256) + 256
         assert fa_lib.fa_bwd_kv_workspace_bytes(B, Hq, Hkv, Sq, Skv, d) == want
     assert fa_lib.fa_bwd_kv_workspace_bytes(1, 2, 2, 128, 0, 64) == 0
     assert fa_lib.fa_bwd_kv_workspace_bytes(1, 2, 2, 128, 128, 64) == \
