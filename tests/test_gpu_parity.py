@@ -165,6 +165,35 @@ def test_repeat_calls_same_result(fa):
     assert np.abs(a["dq"] - b["dq"]).max() <= 1e-2 * np.abs(a["dq"]).max()
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp16", 64)])
+def test_backward_workspace_garbage_and_reuse(fa, dtype, d):
+    """The workspace's contents on entry do not matter: filled with 0xFF bytes
+    (the dQ accumulator, the row vectors and the counter from which the
+    persistent backward's CTAs claim key-tile items), then reused by a second
+    call, every result matches the oracle, and the two calls agree (dK, dV
+    bit for bit). 4 x 8 heads x 10 key tiles = 320 items, more than one per
+    SM."""
+    B, H, S = 4, 8, 1280
+    q, k, v, do = fa_inputs.make_custom(B, H, H, S, d, dtype, seed=320 + d)
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    out, lse = fa.attention_forward(qd, kd, vd, True, scale)
+    ws = fa.workspace_for(qd, kd)
+    ws.fill_(0xFF)
+    first = [f64(t) for t in fa.attention_backward(qd, kd, vd, out, dod, lse, True, scale, ws)]
+    second = [f64(t) for t in fa.attention_backward(qd, kd, vd, out, dod, lse, True, scale, ws)]
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    Q, K, V, DO = map(f64, (q, k, v, do))
+    refs = oracle.backward(Q, K, V, DO, True, scale)
+    for got in (first, second):
+        for name, g, r in zip(("dq", "dk", "dv"), got, refs):
+            check_grad(name, g, r)
+    assert np.array_equal(first[1], second[1]) and np.array_equal(first[2], second[2])
+    assert np.abs(first[0] - second[0]).max() <= 1e-2 * np.abs(first[0]).max()
+
+
 # ------------------------------------------------------------ large sizes --
 def test_longest_sequence_sampled(fa):
     """S = 65536 (twice the longest workload), one head, d = 64: forward and dQ
