@@ -349,11 +349,19 @@ def _calls_for(fa, w, dev):
     return fwd, bwd, nbytes
 
 
+# GPU-side wait queued ahead of a timed call's start event, so that the host
+# issues the call while the GPU is still busy: the events then bracket the
+# call's device time alone (~50 us at 2 GHz, above any call's host time)
+HOST_COVER_CYCLES = 100_000
+
+
 def time_config(fa, w, dev, peaks, warm=10, calls=30, forward_only=False):
     """Per-call CUDA-event times (median over `calls`) of the workload's
     forward and backward entry points, with its roofline against the measured
     peaks. Inputs smaller than L2 get an L2 flush (a 256 MiB write) before
-    every timed call; larger ones need none."""
+    every timed call; larger ones need none. A short GPU-side wait before the
+    start event covers the call's host issue time, which is reported apart
+    (`host_us`, the Python binding plus the C entry point)."""
     import torch
     fwd, bwd, nbytes = _calls_for(fa, w, dev)
     flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if nbytes <= L2_BYTES else None
@@ -370,18 +378,21 @@ def time_config(fa, w, dev, peaks, warm=10, calls=30, forward_only=False):
         for _ in range(warm):
             fn()
         torch.cuda.synchronize(dev)
-        ts = []
+        ts, hs = [], []
         for _ in range(calls):
             if flush is not None:
                 flush.fill_(1)
+            torch.cuda._sleep(HOST_COVER_CYCLES)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
+            t0 = time.perf_counter()
             fn()
+            hs.append((time.perf_counter() - t0) * 1e6)
             b.record()
             b.synchronize()
             ts.append(a.elapsed_time(b))
         ms = statistics.median(ts)
-        entry = {"ms": ms, "ms_mean": statistics.mean(ts)}
+        entry = {"ms": ms, "ms_mean": statistics.mean(ts), "host_us": statistics.median(hs)}
         if w.decode:   # HBM-bound: the split-KV forward streams K and V once
             gbs = nb / (ms * 1e-3) / 1e9
             entry.update({"bound": "hbm", "achieved_gbs": gbs, "frac": gbs / hbm,

@@ -92,8 +92,18 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream):
+# the current stream's raw handle straight from PyTorch's C layer, where the
+# build has it (a cheap call; torch.cuda.current_stream() builds a Stream object)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_NULL_CONTEXT = contextlib.nullcontext()
+
+
+def _stream(stream, t=None):
+    """The CUDA stream handle for a call: `stream` itself, or PyTorch's current
+    stream on t's device (the current device when t is None)."""
     if stream is None:
+        if _raw_stream is not None and t is not None and t.is_cuda:
+            return _raw_stream(t.get_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -118,11 +128,11 @@ def _dims_kv(q, k):
 
 
 def _on_device(t):
-    """Make t's GPU the current device for the call: the library runs on the
-    current device, and the default stream is taken on it."""
-    if t is not None and t.is_cuda:
+    """Make t's GPU the current device for the call (the library runs on the
+    current device); nothing to switch when it already is."""
+    if t is not None and t.is_cuda and t.get_device() != torch.cuda.current_device():
         return torch.cuda.device(t.device)
-    return contextlib.nullcontext()
+    return _NULL_CONTEXT
 
 
 def _check_contig(*ts):
@@ -138,7 +148,7 @@ def fa_fwd(q, k, v, out, lse, causal=True, scale=None, stream=None):
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     with _on_device(q):
         rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, d,
-                          int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), _stream(stream))
+                          int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_fwd")
 
@@ -158,7 +168,7 @@ def fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale=No
     with _on_device(q):
         rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
                           _ptr(dk), _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale,
-                          DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes, _stream(stream))
+                          DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes, _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_bwd")
 
@@ -172,7 +182,7 @@ def fa_fwd_kv(q, k, v, out, lse, causal=True, scale=None, stream=None):
     with _on_device(q):
         rc = lib().fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Skv,
                              d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
-                             _stream(stream))
+                             _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_fwd_kv")
 
@@ -192,7 +202,7 @@ def fa_bwd_kv(q, k, v, out, dout, lse, dq, dk, dv, workspace, causal=True, scale
         rc = lib().fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
                              _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)), scale,
                              DTYPE_CODES.get(q.dtype, -1), _ptr(workspace), ws_bytes,
-                             _stream(stream))
+                             _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_bwd_kv")
 
@@ -213,7 +223,7 @@ def fa_fwd_splitkv(q, k, v, out, lse, causal=True, scale=None, n_splits=0, works
     with _on_device(q):
         rc = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq,
                                   Skv, d, int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1),
-                                  int(n_splits), _ptr(workspace), ws_bytes, _stream(stream))
+                                  int(n_splits), _ptr(workspace), ws_bytes, _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_fwd_splitkv")
 
@@ -249,7 +259,7 @@ def fa_fwd_splitkv_paged(q, k_cache, v_cache, block_table, out, lse, Skv, causal
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(out), _ptr(lse), B, Hq,
             Hkv, Sq, int(Skv), d, block_size, num_blocks, int(block_table.shape[1]),
             int(bool(causal)), scale, DTYPE_CODES.get(q.dtype, -1), int(n_splits), _ptr(workspace),
-            ws_bytes, _stream(stream))
+            ws_bytes, _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_fwd_splitkv_paged")
 
@@ -327,6 +337,6 @@ def fa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, causal=True, scale=None,
     with _on_device(q):   # the scratch array used is the current device's
         rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
                 _ptr(dv), B, Hq, Hkv, S, d, int(bool(causal)), scale,
-                DTYPE_CODES.get(q.dtype, -1), _stream(stream))
+                DTYPE_CODES.get(q.dtype, -1), _stream(stream, q))
     if rc != 0:
         raise FAError(rc, "fa_bwd_noalloc")
