@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float c = p.scale_log2;
 
     Tracer tr(((warp == 2 || warp == 6) && lane == 0) ? p.trace : nullptr, 2 + t);
+    unsigned n_rescale = 0;    // steps that rescaled O (trace builds record it)
     float m_ref = -INFINITY;   // reference max, scaled log2 domain
     float l = 0.f;
     bool ok = true;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // O <- alpha * O for rows whose reference max moved (not needed for the
       // first tile: its P V overwrites O)
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
+        ++n_rescale;
         ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (j - 1) & 1, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
@@ -381,6 +383,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tr(61);
     }
 
+    if (lane == 0 && quarter == 2) trace_span(p.trace, 5 + 2 * t, n_rescale);
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (n - 1) & 1, abort_flag, p.status));
       if (warp == 2 && lane == 0) trace_span(p.trace, 4, clock64());
