@@ -38,8 +38,9 @@
 // three slots each at d = 64), warp 1 MMA issuer and TMEM
 // owner, warps 2-9 compute P^T and dS^T (one thread per key row, two warps per
 // TMEM lane quarter splitting the step's 128 query columns) and then move
-// their half of dQ from TMEM into the global accumulator; at the end warps
-// 2-5 write dK and warps 6-9 write dV.
+// their half of dQ from TMEM into the global accumulator; at the end of an
+// item warps 2-5 write dK and warps 6-9 write dV (bulk tensor stores staged
+// in shared memory the warp owns).
 //
 // Tensor memory: dK [0,d), dV [128,128+d), S^T / P^T [256,384),
 // dP^T / dQ [384,512). dQ reuses dP^T's columns once the softmax warps have
