@@ -100,12 +100,15 @@ int check_common(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, flo
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_SHAPE;
   if (causal && Skv < Sq) return FA_ERR_SHAPE;
-  // grid and index ranges: B*Hq*ceil(Sq/256) forward CTAs, B*Hkv*ceil(Skv/128)
-  // backward CTAs, element offsets in 64 bits
+  // grid and index ranges: B*Hq*ceil(Sq/256) forward CTAs; B*Hkv*ceil(Skv/128)
+  // backward work items, claimed from a 32-bit counter that runs past the
+  // last item by at most one claim per CTA (so the bound keeps 2^16 of
+  // headroom); element offsets in 64 bits
   const long long bh = static_cast<long long>(B) * Hq;
   const long long bhkv = static_cast<long long>(B) * Hkv;
   if (bh > (1LL << 30) || Sq > (1 << 30) || Skv > (1 << 30) ||
-      bh * ((Sq + 255) / 256) > 0x7fffffffLL || bhkv * ((Skv + 127) / 128) > 0x7fffffffLL)
+      bh * ((Sq + 255) / 256) > 0x7fffffffLL ||
+      bhkv * ((Skv + 127) / 128) > 0x7fffffffLL - 0xffffLL)
     return FA_ERR_SHAPE;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_SCALE;
   return FA_OK;

@@ -146,6 +146,16 @@ def test_bwd_kv_rejects_bad_arguments(fa_lib, kw, code):
     assert _bwd_kv(fa_lib.lib(), **kw) == code
 
 
+def test_backward_item_count_bound(fa_lib):
+    """The backward's work items (batch x key/value heads x 128-key tiles) are
+    claimed from a 32-bit counter that runs past the last item by one claim
+    per CTA: sizes within 2^16 of 2^31 are rejected, smaller ones accepted."""
+    H = 1 << 24
+    assert fa_lib.fa_bwd_kv_workspace_bytes(1, H, H, 1, 128 * 128, 64) == 0       # 2^31 items
+    assert fa_lib.fa_bwd_kv_workspace_bytes(1, H, H, 1, 128 * 127 + 1, 64) == 0   # 2^31 items
+    assert fa_lib.fa_bwd_kv_workspace_bytes(1, H, H, 1, 128 * 127, 64) > 0        # 2^31 - 2^24
+
+
 def test_kv_workspace_is_sized_by_the_query_length(fa_lib):
     up = lambda x, m: (x + m - 1) // m * m
     for B, Hq, Hkv, Sq, Skv, d in [(1, 32, 8, 2048, 8192, 128), (2, 4, 2, 1, 777, 64),
