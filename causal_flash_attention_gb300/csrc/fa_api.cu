@@ -100,14 +100,14 @@ int check_common(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, flo
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || Hq % Hkv != 0) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_SHAPE;
   if (causal && Skv < Sq) return FA_ERR_SHAPE;
-  // grid and index ranges: B*Hq*ceil(Sq/256) forward CTAs; B*Hkv*ceil(Skv/128)
+  // grid and index ranges: up to B*Hq*ceil(Sq/128) forward CTAs; B*Hkv*ceil(Skv/128)
   // backward work items, claimed from a 32-bit counter that runs past the
   // last item by at most one claim per CTA (so the bound keeps 2^16 of
   // headroom); element offsets in 64 bits
   const long long bh = static_cast<long long>(B) * Hq;
   const long long bhkv = static_cast<long long>(B) * Hkv;
   if (bh > (1LL << 30) || Sq > (1 << 30) || Skv > (1 << 30) ||
-      bh * ((Sq + 255) / 256) > 0x7fffffffLL ||
+      bh * ((Sq + 127) / 128) > 0x7fffffffLL ||
       bhkv * ((Skv + 127) / 128) > 0x7fffffffLL - 0xffffLL)
     return FA_ERR_SHAPE;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_SCALE;
@@ -266,7 +266,6 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* out, float* lse
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.kv_offset = kv_offset;
   p.causal = causal != 0;
   p.scale_log2 = scale * kLog2e;
-  p.n_qpairs = (Sq + 2 * kTileM - 1) / (2 * kTileM);
   p.kv_tiles_ahead = 1 + (kv_offset + kTileN - 1) / kTileN;
   p.trace = FA_TRACE_PTR;
   p.status = status_ptr();

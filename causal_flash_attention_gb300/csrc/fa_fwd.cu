@@ -8,35 +8,40 @@
 // sum l and an accumulator O per query row, rescaling O and l by exp(m_old -
 // m_new) when the max grows; out = O / l and LSE = m + log l at the end.
 //
-// One CTA owns two 128-row query tiles of one (batch, query head) and walks
-// the key/value tiles up to the causal diagonal (tiles wholly above it are
-// never loaded; "Phase 14", section Causal Mask, tile-level skip). With Sq
-// queries against Skv >= Sq keys, query row i stands at position
-// i + (Skv - Sq), the kv_offset of the same section. Key/value head = query
-// head / (Hq / Hkv) ("Phase 14", section GQA 支持).
+// A CTA owns T = 1 or 2 consecutive 128-row query tiles of one (batch, query
+// head) and walks the key/value tiles up to the causal diagonal (tiles wholly
+// above it are never loaded; "Phase 14", section Causal Mask, tile-level
+// skip). With Sq queries against Skv >= Sq keys, query row i stands at
+// position i + (Skv - Sq), the kv_offset of the same section. Key/value head
+// = query head / (Hq / Hkv) ("Phase 14", section GQA 支持).
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles into two
+// Warp roles (64 + 128 T threads):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles into
 //               multi-stage rings (mbarrier full/empty handshakes).
 //   warp 1      tcgen05 MMA issuer (one thread) and TMEM owner:
 //               S_t = Q_t K_j^T (both operands from shared memory) and
 //               O_t += P_t V_j (P_t from tensor memory, V_j from shared memory).
-//   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1: one
-//               thread per query row reads its score row from TMEM, applies
-//               the causal mask inline, does the online-softmax update with
-//               ex2, writes P (bf16/fp16) back to TMEM over its own scores,
-//               rescales O in TMEM when the row max grew by more than 2^8,
-//               and finally writes out = O / l and LSE.
+//   warps 2-5   softmax for query tile 0 (T = 2: warps 6-9 for query tile 1):
+//               one thread per query row reads its score row from TMEM,
+//               applies the causal mask inline, does the online-softmax update
+//               with ex2, writes P (bf16/fp16) back to TMEM over its own
+//               scores, rescales O in TMEM when the row max grew by more than
+//               2^8, and finally writes out = O / l and LSE.
 //
-// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
-// O_1 [384,384+d). P_t is packed two 16-bit values per column into the first
-// 64 columns of S_t, so the next S_t = Q_t K^T may only be issued after the
+// Tensor memory (256 T columns): S_t [128 t, 128 t + 128), O_t [128 T + 128 t,
+// ... + d). P_t is packed two 16-bit values per column into the first 64
+// columns of S_t, so the next S_t = Q_t K^T may only be issued after the
 // P_t V MMA that reads it has completed (tcgen05 MMAs with different
 // accumulators are not ordered); the issuer waits for that completion.
 //
-// The two softmax groups ping-pong: while one group works on its score tile,
-// the tensor core runs the other tile's P V and Q K^T.
+// T = 2: the two softmax groups ping-pong inside the CTA: while one works on
+// its score tile, the tensor core runs the other tile's P V and Q K^T.
+// T = 1: the CTA is small enough (half the tensor memory, one-stage (d = 128)
+// or two-stage (d = 64) K and V rings) for two to share an SM, and the two
+// CTAs overlap each other's softmax, loads, start-up and write-out the same
+// way; the launcher takes it for grids of at least four one-tile CTAs per SM.
 #include <algorithm>
+#include <cstdlib>
 #include <type_traits>
 
 #include "fa_internal.h"
@@ -45,20 +50,23 @@
 namespace fa {
 namespace {
 
-constexpr int kFwdThreads = 320;
 constexpr float kLn2 = 0.6931471805599453f;
 // A row's reference max only moves when the running max exceeds it by more
 // than this many powers of two; until then p = 2^(x - m_ref) <= 2^8, which
 // fp32 accumulation and 16-bit P both hold without loss of range.
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, int T>
 struct FwdCfg {
+  static constexpr int kTiles = T;                          // query tiles per CTA
+  static constexpr int kThreads = 64 + 128 * T;
+  static constexpr int kTmemCols = 256 * T;
   static constexpr int kChunks = D / kChunk;                // 64-col chunks per row
   static constexpr int kTileBytes = kTileM * D * 2;         // one 128 x D tile
-  static constexpr int kStages = (D == 128) ? 2 : 3;        // K ring and V ring depth
-  static constexpr int kOffQ = 0;                           // 2 Q tiles
-  static constexpr int kOffK = 2 * kTileBytes;
+  // K ring and V ring depth (one tile per CTA: small enough for two CTAs per SM)
+  static constexpr int kStages = T == 2 ? ((D == 128) ? 2 : 3) : ((D == 128) ? 1 : 2);
+  static constexpr int kOffQ = 0;                           // T Q tiles
+  static constexpr int kOffK = T * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
@@ -91,10 +99,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   }
 }
 
-template <int D, bool kBf16>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+template <int D, bool kBf16, int T>
+__global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using Cfg = FwdCfg<D>;
+  using Cfg = FwdCfg<D, T>;
   constexpr int NS = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -118,9 +126,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
 
-  // ---- work assignment: heaviest query-tile pairs first (causal) ----
+  // ---- work assignment: T consecutive query tiles, heaviest units first (causal) ----
   const int BHq = p.B * p.Hq;
-  const int pair = p.n_qpairs - 1 - static_cast<int>(blockIdx.x) / BHq;
+  const int unit = p.n_units - 1 - static_cast<int>(blockIdx.x) / BHq;
   const int bh = static_cast<int>(blockIdx.x) % BHq;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int bkv = b * p.Hkv + hq / (p.Hq / p.Hkv);
@@ -129,10 +137,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // below q_end + kv_offset <= Skv, i.e. tiles up to qt + kv_tiles_ahead for a
   // full tile and every tile for the last, ragged one.
   const int n_kv_total = (p.Skv + kTileN - 1) / kTileN;
-  int n_t[2];
+  int n_t[2] = {0, 0};
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int q0 = pair * 2 * kTileM + t * kTileM;
+  for (int t = 0; t < T; ++t) {
+    const int q0 = unit * T * kTileM + t * kTileM;
     if (q0 >= p.Sq) n_t[t] = 0;
     else n_t[t] = p.causal ? min(q0 / kTileN + p.kv_tiles_ahead, n_kv_total) : n_kv_total;
   }
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -178,9 +186,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t q_bytes = (n_t[0] > 0 ? Cfg::kTileBytes : 0) + (n_t[1] > 0 ? Cfg::kTileBytes : 0);
       if (q_bytes) {
         mbar_arrive_expect_tx(bars.q_full, q_bytes);
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < T; ++t) {
           if (n_t[t] == 0) continue;
-          const int q0 = pair * 2 * kTileM + t * kTileM;
+          const int q0 = unit * T * kTileM + t * kTileM;
           for (int c = 0; c < Cfg::kChunks; ++c)
             tma_load_3d(sbase + Cfg::kOffQ + t * Cfg::kTileBytes + c * (kTileM * 128), &p.tm_q,
                         bars.q_full, c * kChunk, q0, bh);
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       auto issue_pv = [&](int t, int st, bool accumulate) {   // O_t (+)= P_t V
         const uint64_t vb =
             make_sdesc(sbase + Cfg::kOffV + st * Cfg::kTileBytes, kTileN * 128, 1024);
-        mma_ts_product8<false, 0>(tmem + 256 + t * 128, tmem + t * 128, vb, idesc_pv,
+        mma_ts_product8<false, 0>(tmem + 128 * T + t * 128, tmem + t * 128, vb, idesc_pv,
                                   accumulate ? 1u : 0u);
         tc_commit(bars.pv(t));
       };
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tr(9);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < T; ++t)
           if (n_t[t] > 0) issue_qk(t, 0);
         tc_commit(bars.ke(0));
       }
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int st = j % NS;
         const uint32_t par = static_cast<uint32_t>(j / NS) & 1;
         if (!(ok = mbar_wait(bars.vf(st), par, abort_flag, p.status))) break;
-        for (int t = 0; t < 2 && ok; ++t) {
+        for (int t = 0; t < T && ok; ++t) {
           if (j >= n_t[t]) continue;
           if (!(ok = mbar_wait(bars.pf(t), j & 1, abort_flag, p.status))) break;
           tr(50 + t);
@@ -287,12 +295,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int t = (warp - 2) / 4;               // query tile of this warp group
     const int quarter = warp & 3;               // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;          // row within the tile
-    const int q0 = pair * 2 * kTileM + t * kTileM;
+    const int q0 = unit * T * kTileM + t * kTileM;
     const int row = q0 + r;
     const int n = n_t[t];
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + t * 128;
-    const uint32_t o_tmem = tmem + lane_off + 256 + t * 128;
+    const uint32_t o_tmem = tmem + lane_off + 128 * T + t * 128;
     const float c = p.scale_log2;
 
     Tracer tr(((warp == 2 || warp == 6) && lane == 0) ? p.trace : nullptr, 2 + t);
@@ -420,26 +428,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (threadIdx.x == 0) trace_span(p.trace, 6, clock64());
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, Cfg::kTmemCols);
   }
 }
 
-template <int D, bool kBf16>
-cudaError_t launch_fwd_impl(const FwdParams& p, cudaStream_t stream) {
-  constexpr int smem = FwdCfg<D>::kSmemBytes;
-  auto kernel = fa_fwd_kernel<D, kBf16>;
+template <int D, bool kBf16, int T>
+cudaError_t launch_fwd_impl(const FwdParams& p0, cudaStream_t stream) {
+  constexpr int smem = FwdCfg<D, T>::kSmemBytes;
+  auto kernel = fa_fwd_kernel<D, kBf16, T>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.B * p.Hq * p.n_qpairs);
-  kernel<<<grid, kFwdThreads, smem, stream>>>(p);
+  FwdParams p = p0;
+  p.n_units = (p.Sq + T * kTileM - 1) / (T * kTileM);   // T query tiles per CTA
+  const unsigned grid =
+      static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * p.n_units);   // < 2^31
+  kernel<<<grid, FwdCfg<D, T>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+// One query tile per CTA when the grid has at least kOneTileWaves one-tile
+// CTAs per SM (two co-reside per SM and overlap each other's loads, softmax
+// and start-up), else two tiles per CTA (ping-pong inside the CTA, which a
+// lone CTA in a grid's last wave still has). FA_FWD_TILES=1 or 2 in the
+// environment forces one form for every call; both compute the same bits.
+constexpr int kOneTileWaves = 4;
+
+template <int D, bool kBf16>
+cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+  int tiles = 0;
+  const char* env = std::getenv("FA_FWD_TILES");
+  if (env && (env[0] == '1' || env[0] == '2') && env[1] == 0) tiles = env[0] - '0';
+  if (tiles == 0) {
+    int dev = 0, n_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long one_tile_ctas =
+        static_cast<long long>(p.B) * p.Hq * ((p.Sq + kTileM - 1) / kTileM);
+    tiles = one_tile_ctas >= static_cast<long long>(kOneTileWaves) * n_sm ? 1 : 2;
+  }
+  return tiles == 1 ? launch_fwd_impl<D, kBf16, 1>(p, stream) : launch_fwd_impl<D, kBf16, 2>(p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdParams& p, int d, bool bf16, cudaStream_t stream) {
-  if (d == 128) return bf16 ? launch_fwd_impl<128, true>(p, stream) : launch_fwd_impl<128, false>(p, stream);
-  return bf16 ? launch_fwd_impl<64, true>(p, stream) : launch_fwd_impl<64, false>(p, stream);
+  if (d == 128) return bf16 ? launch_fwd_d<128, true>(p, stream) : launch_fwd_d<128, false>(p, stream);
+  return bf16 ? launch_fwd_d<64, true>(p, stream) : launch_fwd_d<64, false>(p, stream);
 }
 
 }  // namespace fa

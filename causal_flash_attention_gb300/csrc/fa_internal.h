@@ -27,7 +27,8 @@ struct FwdParams {
   int B, Hq, Hkv, Sq, Skv, kv_offset;
   int causal;
   float scale_log2;   // softmax scale * log2(e)
-  int n_qpairs;       // ceil(Sq / 256): CTAs per (batch, query head)
+  int n_units;        // CTAs per (batch, query head): ceil(Sq / (128 T)) for T query
+                      // tiles per CTA (set by the forward's launcher)
   int kv_tiles_ahead; // 1 + ceil(kv_offset / 128): key tiles a full causal
                       // query tile qt walks is qt + kv_tiles_ahead
   int* status;        // device status word (wait timeouts)
