@@ -33,13 +33,18 @@
 // columns of S_t, so the next S_t = Q_t K^T may only be issued after the
 // P_t V MMA that reads it has completed (tcgen05 MMAs with different
 // accumulators are not ordered); the issuer waits for that completion.
+// Except at d = 64 with T = 1, where P has its own 64 columns after O (256
+// columns in all): there the softmax warps release S as soon as they have
+// read it, the issuer starts the next S = Q K^T at once, and the warps wait
+// for the previous P V only before writing the new P.
 //
 // T = 2: the two softmax groups ping-pong inside the CTA: while one works on
 // its score tile, the tensor core runs the other tile's P V and Q K^T.
 // T = 1: the CTA is small enough (half the tensor memory, one-stage (d = 128)
 // or two-stage (d = 64) K and V rings) for two to share an SM, and the two
 // CTAs overlap each other's softmax, loads, start-up and write-out the same
-// way; the launcher takes it for grids of at least four one-tile CTAs per SM.
+// way; the launcher takes it for grids of at least four one-tile CTAs per SM,
+// and for every grid at d = 64.
 #include <algorithm>
 #include <cstdlib>
 #include <type_traits>
@@ -61,6 +66,10 @@ struct FwdCfg {
   static constexpr int kTiles = T;                          // query tiles per CTA
   static constexpr int kThreads = 64 + 128 * T;
   static constexpr int kTmemCols = 256 * T;
+  // d = 64, one tile: P gets its own 64 columns after O (free at that d),
+  // so the next S = Q K^T may be issued as soon as S has been read out of
+  // TMEM, and runs during the softmax and P V of the current tile
+  static constexpr bool kSepP = (D == 64 && T == 1);
   static constexpr int kChunks = D / kChunk;                // 64-col chunks per row
   static constexpr int kTileBytes = kTileM * D * 2;         // one 128 x D tile
   // K ring and V ring depth (one tile per CTA: small enough for two CTAs per SM)
@@ -70,14 +79,14 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[2], p_full[2], pv_done[2], drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+  //           s_full[2], p_full[2], pv_done[2], drain, (kSepP) s_free[2]
+  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1 + (kSepP ? 2 : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 };
 
 struct FwdBars {
-  uint32_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, drain;
+  uint32_t q_full, k_full, k_empty, v_full, v_empty, s_full, p_full, pv_done, drain, s_free;
   int stages;
   __device__ uint32_t kf(int s) const { return k_full + 8 * s; }
   __device__ uint32_t ke(int s) const { return k_empty + 8 * s; }
@@ -86,6 +95,7 @@ struct FwdBars {
   __device__ uint32_t sf(int t) const { return s_full + 8 * t; }
   __device__ uint32_t pf(int t) const { return p_full + 8 * t; }
   __device__ uint32_t pv(int t) const { return pv_done + 8 * t; }
+  __device__ uint32_t sfr(int t) const { return s_free + 8 * t; }
 };
 
 // Bounded wait used on the abort path: only the limit can end it.
@@ -122,6 +132,7 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
   bars.p_full = bars.s_full + 16;
   bars.pv_done = bars.p_full + 16;
   bars.drain = bars.pv_done + 16;
+  bars.s_free = bars.drain + 8;
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
@@ -164,6 +175,7 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
       mbar_init(bars.pf(t), 4);   // one arrival per softmax warp
       mbar_init(bars.pv(t), 1);
     }
+    if (Cfg::kSepP) mbar_init(bars.sfr(0), 4);   // one arrival per softmax warp
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -245,7 +257,8 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
       auto issue_pv = [&](int t, int st, bool accumulate) {   // O_t (+)= P_t V
         const uint64_t vb =
             make_sdesc(sbase + Cfg::kOffV + st * Cfg::kTileBytes, kTileN * 128, 1024);
-        mma_ts_product8<false, 0>(tmem + 128 * T + t * 128, tmem + t * 128, vb, idesc_pv,
+        const uint32_t o_t = tmem + 128 * T + t * 128;
+        mma_ts_product8<false, 0>(o_t, Cfg::kSepP ? o_t + D : tmem + t * 128, vb, idesc_pv,
                                   accumulate ? 1u : 0u);
         tc_commit(bars.pv(t));
       };
@@ -262,14 +275,29 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
       for (int j = 0; ok && j < n_load; ++j) {
         const int st = j % NS;
         const uint32_t par = static_cast<uint32_t>(j / NS) & 1;
-        if (!(ok = mbar_wait(bars.vf(st), par, abort_flag, p.status))) break;
+        bool k_next = false, v_cur = false;   // K_{j+1}, V_j seen landed
         for (int t = 0; t < T && ok; ++t) {
+          if constexpr (Cfg::kSepP) {
+            if (j + 1 < n_t[t]) {
+              const int st1 = (j + 1) % NS;
+              const uint32_t par1 = static_cast<uint32_t>((j + 1) / NS) & 1;
+              if (!k_next && !(ok = mbar_wait(bars.kf(st1), par1, abort_flag, p.status))) break;
+              k_next = true;
+              // S_t(j) has been read out of TMEM: S_t(j + 1) may overwrite it
+              if (!(ok = mbar_wait(bars.sfr(t), j & 1, abort_flag, p.status))) break;
+              tr(54 + t);
+              tc_fence_after();
+              issue_qk(t, st1);
+            }
+          }
           if (j >= n_t[t]) continue;
+          if (!v_cur && !(ok = mbar_wait(bars.vf(st), par, abort_flag, p.status))) break;
+          v_cur = true;
           if (!(ok = mbar_wait(bars.pf(t), j & 1, abort_flag, p.status))) break;
           tr(50 + t);
           tc_fence_after();
           issue_pv(t, st, j > 0);
-          if (j + 1 < n_t[t]) {
+          if (!Cfg::kSepP && j + 1 < n_t[t]) {
             const int st1 = (j + 1) % NS;
             const uint32_t par1 = static_cast<uint32_t>((j + 1) / NS) & 1;
             if (!(ok = mbar_wait(bars.kf(st1), par1, abort_flag, p.status))) break;
@@ -301,6 +329,7 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + t * 128;
     const uint32_t o_tmem = tmem + lane_off + 128 * T + t * 128;
+    const uint32_t p_tmem = Cfg::kSepP ? o_tmem + D : s_tmem;
     const float c = p.scale_log2;
 
     Tracer tr(((warp == 2 || warp == 6) && lane == 0) ? p.trace : nullptr, 2 + t);
@@ -323,6 +352,11 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < kTileN; ++i) s[i] = __uint_as_float(raw[i]);
+      }
+      if constexpr (Cfg::kSepP) {   // the issuer may overwrite S_t with the next tile's
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.sfr(t));
       }
       const int kv0 = j * kTileN;
       // inline mask: causal (key after the query's position) and keys past the
@@ -362,17 +396,25 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
           sum[(2 * i + 1) & 3] += p1;
           pk[i] = pack2<kBf16>(p0, p1);
         }
-        tmem_st32(s_tmem + h * 32, pk);
+        if (Cfg::kSepP && h == 0 && j > 0) {
+          // P_t(j - 1) V_{j-1} has read the P buffer (and O may be rescaled)
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (j - 1) & 1, abort_flag, p.status));
+          tc_fence_after();
+        }
+        tmem_st32(p_tmem + h * 32, pk);
       }
+      if (!ok) break;
       l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
 
       // O <- alpha * O for rows whose reference max moved (not needed for the
       // first tile: its P V overwrites O)
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
         ++n_rescale;
-        ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (j - 1) & 1, abort_flag, p.status));
-        if (!ok) break;
-        tc_fence_after();
+        if constexpr (!Cfg::kSepP) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bars.pv(t), (j - 1) & 1, abort_flag, p.status));
+          if (!ok) break;
+          tc_fence_after();
+        }
         const float a = moved ? alpha : 1.f;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -449,8 +491,11 @@ cudaError_t launch_fwd_impl(const FwdParams& p0, cudaStream_t stream) {
 // One query tile per CTA when the grid has at least kOneTileWaves one-tile
 // CTAs per SM (two co-reside per SM and overlap each other's loads, softmax
 // and start-up), else two tiles per CTA (ping-pong inside the CTA, which a
-// lone CTA in a grid's last wave still has). FA_FWD_TILES=1 or 2 in the
-// environment forces one form for every call; both compute the same bits.
+// lone CTA in a grid's last wave still has). d = 64 always takes one tile:
+// its separate P buffer lets each CTA overlap the next Q K^T with its own
+// softmax, which beats the two-tile form at every grid size. FA_FWD_TILES=1
+// or 2 in the environment forces one form for every call; both compute the
+// same bits.
 constexpr int kOneTileWaves = 4;
 
 template <int D, bool kBf16>
@@ -458,6 +503,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
   int tiles = 0;
   const char* env = std::getenv("FA_FWD_TILES");
   if (env && (env[0] == '1' || env[0] == '2') && env[1] == 0) tiles = env[0] - '0';
+  if (tiles == 0 && D == 64) tiles = 1;
   if (tiles == 0) {
     int dev = 0, n_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);

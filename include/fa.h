@@ -86,9 +86,10 @@ enum {
  * 硬件约束); both write the same bits. The environment variable
  * FA_FWD_CTA_PAIR, read at every call, selects the pair kernel when it is "1"
  * and the single-CTA kernel when it is "0". The single-CTA kernel gives each
- * CTA one 128-row query tile (two CTAs share an SM) when the grid has at
- * least four such CTAs per SM, else two tiles; FA_FWD_TILES ("1" or "2",
- * read at every call) forces one form. All forms write the same bits.
+ * CTA one 128-row query tile (two CTAs share an SM) at d = 64 and, at
+ * d = 128, when the grid has at least four such CTAs per SM, else two tiles;
+ * FA_FWD_TILES ("1" or "2", read at every call) forces one form. All forms
+ * write the same bits.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
            int B, int Hq, int Hkv, int S, int d, int causal, float scale,
