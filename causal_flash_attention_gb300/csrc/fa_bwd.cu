@@ -45,6 +45,9 @@
 // Tensor memory: dK [0,d), dV [128,128+d), S^T / P^T [256,384),
 // dP^T / dQ [384,512). dQ reuses dP^T's columns once the softmax warps have
 // read dP^T; S^T(i+1) is issued only after dV(i), which reads P^T(i), is done.
+// At d = 64, P^T [64,128) and dQ [192,256) have columns of their own instead:
+// S^T(i+1) is issued once the compute warps have read S^T(i), dP^T(i+1)
+// right after dQ(i), and the warps read dQ(i) out after P^T(i+1).
 #include <algorithm>
 #include <type_traits>
 
@@ -59,6 +62,12 @@ constexpr float kLog2eF = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
+  // d = 64 leaves 128 of the 512 TMEM columns free: packed P^T (64-127) and
+  // dQ (192-255) get their own instead of going over S^T and dP^T. S^T(n+1)
+  // then waits only for S^T(n) to have been read (not for dV(n)), dP^T(n+1)
+  // not for the dQ(n) read-out, and the compute warps read dQ(n) out after
+  // P^T(n+1), by when the product has long completed
+  static constexpr bool kSepQ = (D == 64);
   static constexpr int kChunks = D / kChunk;
   static constexpr int kTileBytes = kTileM * D * 2;        // one 128 x D tile
   // Q_i (with its L and D rows) is live from S^T(i), issued during the step
@@ -79,7 +88,7 @@ struct BwdCfg {
   static constexpr int kOffBar = kOffRow + kQStages * 1024;
   // kv_full, kv_empty, q_full[NQ], q_empty[NQ], do_full[ND], do_empty[ND], s_full,
   // dp_full, p_full, ds_full, dv_done, dq_full, dq_empty, ds_empty, kd_done, drain
-  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 10;
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 10 + (kSepQ ? 1 : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16;
 };
@@ -245,6 +254,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t ds_empty = s_full + 56;
   const uint32_t kd_done = s_full + 64;
   const uint32_t drain = s_full + 72;
+  const uint32_t s_free = s_full + 80;   // kSepQ: the compute warps have read S^T
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
@@ -275,6 +285,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(ds_empty, 1);
     mbar_init(kd_done, 1);
     mbar_init(drain, 1);
+    if (Cfg::kSepQ) mbar_init(s_free, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -393,6 +404,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // follow soon after dS(n); S^T(n+1) as soon as dV(n) has read P^T(n)):
     //   dV(n) [P(n) ready]  dQ(n) [dS(n) ready]  S^T(n+1) [dV(n) done]
     //   dK(n)  dP^T(n+1) [dQ(n) read out of TMEM]
+    // d = 64 (own P^T and dQ columns):
+    //   S^T(n+1) [S^T(n) read]  dV(n) [P(n) ready]
+    //   dQ(n) [dS(n) ready, dQ(n-1) read out]  dP^T(n+1)  dK(n)
     // After an item's last step: kv_empty (K, V read for the last time by
     // that dQ), dK, kd_done; the next item's S^T and dP^T once its K, V land.
     if (lane == 0) {
@@ -400,6 +414,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_kv = make_idesc(128, D, kBf16, false, true);       // dV, dK
       constexpr uint32_t idesc_q = make_idesc(128, D, kBf16, true, true);         // dQ
       const uint32_t t_dk = tmem, t_dv = tmem + 128, t_s = tmem + 256, t_dp = tmem + 384;
+      const uint32_t t_dq = Cfg::kSepQ ? tmem + 192 : t_dp;
+      const uint32_t t_p = Cfg::kSepQ ? tmem + 64 : t_s;   // packed P^T
       const uint32_t k_s = sbase + Cfg::kOffK, v_s = sbase + Cfg::kOffV;
       const uint32_t ds_s = sbase + Cfg::kOffDS;
       auto q_s = [&](int st) { return sbase + Cfg::kOffQ + st * Cfg::kTileBytes; };
@@ -433,7 +449,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_s = [&](int g) -> bool {
         if (!mbar_wait(q_full(g % NQ), static_cast<uint32_t>(g / NQ) & 1, abort_flag, p.status))
           return false;
-        if (g > 0 && !mbar_wait(dv_done, (g - 1) & 1, abort_flag, p.status)) return false;
+        if (g > 0 && !mbar_wait(Cfg::kSepQ ? s_free : dv_done, (g - 1) & 1, abort_flag, p.status))
+          return false;
         tr(5);
         tc_fence_after();
         mma_ss_product<D / 16, true, kCB, true, kCB>(t_s, k_desc, q_desc(g % NQ), idesc_s, 0);
@@ -442,7 +459,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       // dP^T(g) = V_j dO_i^T once dO_i has landed and dQ(g-1) has left TMEM
       auto issue_dp = [&](int g) -> bool {
-        if (g > 0 && !mbar_wait(dq_empty, (g - 1) & 1, abort_flag, p.status)) return false;
+        if (!Cfg::kSepQ && g > 0 && !mbar_wait(dq_empty, (g - 1) & 1, abort_flag, p.status))
+          return false;
         if (!mbar_wait(do_full(g % ND), static_cast<uint32_t>(g / ND) & 1, abort_flag, p.status))
           return false;
         tr(7);
@@ -471,6 +489,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int st = g % NQ;
           const int sd = g % ND;
           const bool more = n + 1 < N;
+          if constexpr (Cfg::kSepQ) {
+            // S^T(n+1) as soon as the compute warps have read S^T(n)
+            if (more && !(ok = issue_s(g + 1))) break;
+            // dV += P^T dO_i (P^T packed in its own columns)
+            if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
+            tr(1);
+            tc_fence_after();
+            mma_ts_product8<false, 0>(t_dv, t_p, do_desc_mn(sd), idesc_kv, n > 0 ? 1u : 0u);
+            tc_commit(dv_done);
+            tc_commit(do_empty(sd));
+            // dS^T(n) written (so dP^T(n) has been read) and dQ(n-1) read out:
+            // dQ(n), dP^T(n+1), dK(n)
+            if (!(ok = mbar_wait(ds_full, g & 1, abort_flag, p.status))) break;
+            tr(3);
+            if (g > 0 && !(ok = mbar_wait(dq_empty, (g - 1) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            mma_ss_product<kTileN / 16, false, 0, false, 0>(t_dq, ds_desc_mn, k_desc_mn, idesc_q, 0);
+            tc_commit(dq_full);
+            if (!more) tc_commit(kv_empty);
+            if (more && !(ok = issue_dp(g + 1))) break;
+            mma_ss_product<kTileM / 16, true, kCB, false, 0>(t_dk, ds_desc, q_desc_mn(st), idesc_kv,
+                                                            n > 0 ? 1u : 0u);
+            tc_commit(ds_empty);
+            tc_commit(q_empty(st));
+            tr(6);
+            continue;
+          }
           // dV += P^T dO_i  (P^T from TMEM, 16-bit packed: query columns 0-63 in
           // S^T's columns 0-31, columns 64-127 in S^T's columns 96-127)
           if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
@@ -484,7 +529,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tr(3);
           tc_fence_after();
           // dQ = dS K_j, both operands MN-major
-          mma_ss_product<kTileN / 16, false, 0, false, 0>(t_dp, ds_desc_mn, k_desc_mn, idesc_q, 0);
+          mma_ss_product<kTileN / 16, false, 0, false, 0>(t_dq, ds_desc_mn, k_desc_mn, idesc_q, 0);
           tc_commit(dq_full);
           // S^T for the next step of this item; after its last step K and V
           // are free for the next item's
@@ -518,7 +563,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // query columns 0-63 of the step (half 0), warps 6-9 columns 64-127
     // (half 1). Each warp writes its packed P^T over score columns it has
     // read itself (half 0: columns 0-31, half 1: 96-127), so the two warps of
-    // a quarter never wait for each other.
+    // a quarter never wait for each other; at d = 64 into the P^T buffer's
+    // columns [32 half, 32 half + 32) once dV has read the previous P^T.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int c0 = half * 64;                   // first query column of this warp
@@ -526,6 +572,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + 256;
     const uint32_t t_dp = tmem + lane_off + 384;
+    const uint32_t t_dq = Cfg::kSepQ ? tmem + lane_off + 192 : t_dp;
+    const uint32_t t_p = Cfg::kSepQ ? tmem + lane_off + 64 : t_s;
     const float c = p.scale_log2;
     // dS^T row r of 64-column chunk `half` of the 128-byte-swizzled tile
     uint8_t* ds_row = smem + Cfg::kOffDS + half * (kTileN * 128) + r * 128;
@@ -559,6 +607,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bulk_commit_group();
       }
     };
+    // dQ of step gg (query tile ii, head bhh): TMEM -> fp32 accumulator. This
+    // thread holds head-dimension entries [half * D/2, (half + 1) * D/2) of
+    // query row r of the tile.
+    auto read_dq = [&](int gg, int ii, int bhh) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, gg & 1, abort_flag, p.status))) return false;
+      tr(30);
+      tc_fence_after();
+      constexpr int kCols = D / 2;
+      uint32_t acc[kCols];
+#pragma unroll
+      for (int cc = 0; cc < kCols / 32; ++cc)
+        tmem_ld32(t_dq + half * kCols + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+      tr(31);
+      if constexpr (D == 128) {
+        reduce_box(acc, half * 64, ii * kTileM + quarter * 32, bhh);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
+        pend_x = half * 64 + 32;
+        pend_y = ii * kTileM + quarter * 32;
+        pend_bh = bhh;
+      } else {   // d = 64: the step's 32 columns are one box
+        reduce_box(acc, half * 32, ii * kTileM + quarter * 32, bhh);
+      }
+      tr(32);
+      return true;
+    };
+    int prev_i = 0, prev_bh = 0;   // kSepQ: the step whose dQ is still to be read out
     int g = 0;   // global step
     for (int k = 0; ok; ++k) {
       ok = __all_sync(0xffffffffu, mbar_wait(kv_full, k & 1, abort_flag, p.status));
@@ -593,6 +672,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(raw));
           tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
           tmem_wait_ld();
+          if constexpr (Cfg::kSepQ) {   // S^T(n+1) may overwrite these scores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+          }
           if (any_mask) {
 #pragma unroll
             for (int e = 0; e < 64; ++e) raw[e] = (e < thr) ? __float_as_uint(-INFINITY) : raw[e];
@@ -606,13 +690,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                              f2_pack(-l2.x, -l2.y)), x0, x1);
             ppk[e / 2] = pack2<kBf16>(ex2(x0), ex2(x1));
           }
-          tmem_st32(t_s + half * 96, ppk);
+          if constexpr (Cfg::kSepQ) {
+            // dV(n-1) has read the previous P^T: columns [32 half, 32 half + 32)
+            // of the P^T buffer take this warp's 64 query columns
+            if (g > 0) ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (g - 1) & 1, abort_flag, p.status));
+            tc_fence_after();
+            tmem_st32(t_p + half * 32, ppk);
+          } else {
+            tmem_st32(t_s + half * 96, ppk);
+          }
         }
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
         tr(21);
+        if (Cfg::kSepQ && it > 0 && !(ok = read_dq(g - 1, prev_i, prev_bh))) break;
 
         if (g > 0) ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (g - 1) & 1, abort_flag, p.status));
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, abort_flag, p.status));
@@ -661,34 +755,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tr(34);
         }
 
-        // dQ(it): TMEM -> fp32 accumulator. This thread holds head-dimension
-        // entries [half * D/2, (half + 1) * D/2) of query row r of the tile.
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, p.status));
-        if (!ok) break;
-        tr(30);
-        tc_fence_after();
-        constexpr int kCols = D / 2;
-        uint32_t acc[kCols];
-#pragma unroll
-        for (int cc = 0; cc < kCols / 32; ++cc)
-          tmem_ld32(t_dp + half * kCols + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(acc + cc * 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dq_empty);
-        tr(31);
         const int bh = I.b * p.Hq + I.g * (p.Hq / p.Hkv) + it / I.n_i;
-        if constexpr (D == 128) {
-          reduce_box(acc, half * 64, i * kTileM + quarter * 32, bh);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) dq_pend[q] = acc[32 + q];
-          pend_x = half * 64 + 32;
-          pend_y = i * kTileM + quarter * 32;
-          pend_bh = bh;
-        } else {   // d = 64: the step's 32 columns are one box
-          reduce_box(acc, half * 32, i * kTileM + quarter * 32, bh);
+        if (!Cfg::kSepQ || it + 1 == I.n_iter) {   // else after the next step's P^T
+          if (!(ok = read_dq(g, i, bh))) break;
         }
-        tr(32);
+        prev_i = i;
+        prev_bh = bh;
       }
       if (!ok) break;
       if (pend_x >= 0) reduce_box(dq_pend, pend_x, pend_y, pend_bh);
