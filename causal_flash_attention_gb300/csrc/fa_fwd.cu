@@ -70,6 +70,9 @@ struct FwdCfg {
   // so the next S = Q K^T may be issued as soon as S has been read out of
   // TMEM, and runs during the softmax and P V of the current tile
   static constexpr bool kSepP = (D == 64 && T == 1);
+  // same form: the softmax in paired fp32 instructions and 3-input max (the
+  // registers allow it there; the results are bit-identical to the scalar form)
+  static constexpr bool kPaired = kSepP;
   static constexpr int kChunks = D / kChunk;                // 64-col chunks per row
   static constexpr int kTileBytes = kTileM * D * 2;         // one 128 x D tile
   // K ring and V ring depth (one tile per CTA: small enough for two CTAs per SM)
@@ -369,12 +372,26 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
           if (kv0 + i > lim) s[i] = -INFINITY;
       }
       float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      if constexpr (Cfg::kPaired) {
 #pragma unroll
-      for (int i = 4; i < kTileN; i += 4) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
-        mx2 = fmaxf(mx2, s[i + 2]);
-        mx3 = fmaxf(mx3, s[i + 3]);
+        for (int i = 4; i + 8 <= kTileN; i += 8) {
+          mx0 = fmax3(mx0, s[i], s[i + 4]);
+          mx1 = fmax3(mx1, s[i + 1], s[i + 5]);
+          mx2 = fmax3(mx2, s[i + 2], s[i + 6]);
+          mx3 = fmax3(mx3, s[i + 3], s[i + 7]);
+        }
+        mx0 = fmaxf(mx0, s[kTileN - 4]);
+        mx1 = fmaxf(mx1, s[kTileN - 3]);
+        mx2 = fmaxf(mx2, s[kTileN - 2]);
+        mx3 = fmaxf(mx3, s[kTileN - 1]);
+      } else {
+#pragma unroll
+        for (int i = 4; i < kTileN; i += 4) {
+          mx0 = fmaxf(mx0, s[i]);
+          mx1 = fmaxf(mx1, s[i + 1]);
+          mx2 = fmaxf(mx2, s[i + 2]);
+          mx3 = fmaxf(mx3, s[i + 3]);
+        }
       }
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
       float m_new = m_ref;
@@ -388,13 +405,31 @@ __global__ void __launch_bounds__(FwdCfg<D, T>::kThreads, 3 - T)
       uint32_t pk[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        if constexpr (Cfg::kPaired) {
+          // element e adds into sum[e % 4] as in the scalar form: pairs with
+          // i even into (sum0, sum1), i odd into (sum2, sum3)
+          const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
+          uint64_t s01 = f2_pack(sum[0], sum[1]), s23 = f2_pack(sum[2], sum[3]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[h * 64 + 2 * i], c, -m_use));
-          const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], c, -m_use));
-          sum[(2 * i) & 3] += p0;
-          sum[(2 * i + 1) & 3] += p1;
-          pk[i] = pack2<kBf16>(p0, p1);
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]), c2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            if (i & 1) s23 = f2_add(s23, f2_pack(p0, p1));
+            else s01 = f2_add(s01, f2_pack(p0, p1));
+            pk[i] = pack2<kBf16>(p0, p1);
+          }
+          f2_unpack(s01, sum[0], sum[1]);
+          f2_unpack(s23, sum[2], sum[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2(fmaf(s[h * 64 + 2 * i], c, -m_use));
+            const float p1 = ex2(fmaf(s[h * 64 + 2 * i + 1], c, -m_use));
+            sum[(2 * i) & 3] += p0;
+            sum[(2 * i + 1) & 3] += p1;
+            pk[i] = pack2<kBf16>(p0, p1);
+          }
         }
         if (Cfg::kSepP && h == 0 && j > 0) {
           // P_t(j - 1) V_{j-1} has read the P buffer (and O may be rescaled)
