@@ -355,8 +355,9 @@ def _calls_for(fa, w, dev):
 HOST_COVER_CYCLES = 100_000
 
 
-def time_config(fa, w, dev, peaks, warm=10, calls=30, forward_only=False):
-    """Per-call CUDA-event times (median over `calls`) of the workload's
+def time_config(fa, w, dev, peaks, warm=20, calls=50, forward_only=False):
+    """Per-call CUDA-event times (median over `calls`, after `warm` untimed
+    calls) of the workload's
     forward and backward entry points, with its roofline against the measured
     peaks. Inputs smaller than L2 get an L2 flush (a 256 MiB write) before
     every timed call; larger ones need none. A short GPU-side wait before the
