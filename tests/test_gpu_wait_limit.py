@@ -8,7 +8,8 @@ clears. libfa_waittest.so is the same library built with the wait limit cut to
 about a millisecond and each tensor-core kernel's MMA issuer made to wait
 first for a barrier phase that nothing completes (built by
 causal_flash_attention_gb300.build.build_all). The forward runs in both its
-single-CTA and its CTA-pair form. Nothing faults, traps or
+single-CTA forms (one tile per CTA and two) and its CTA-pair form, and
+both head dimensions' kernels run. Nothing faults, traps or
 hangs: the wait ends at its limit. The test checks that each call returns,
 that the status reports the timeout and is cleared by the read, and that the
 product library, called next in the same process and context, still computes
@@ -94,6 +95,39 @@ def test_wait_that_runs_out_ends_the_kernel_with_an_error_status(fa):
                     dod.data_ptr(), ref_lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                     dv.data_ptr(), B, Hq, Hkv, S, d, 1, scale, 2, ws.data_ptr(), nws,
                     stream) == 0
+    torch.cuda.synchronize(dev)
+    assert _status(L, stream) & STATUS_WAIT_TIMEOUT
+    assert _status(L, stream) == 0
+
+    # the one-tile forward (d = 128, forced) and the d = 64 kernels (the
+    # one-tile forward with its separate P buffer, the backward with its own
+    # P^T and dQ columns): each ends with the timeout reported
+    os.environ["FA_FWD_TILES"] = "1"
+    try:
+        assert L.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(),
+                        lse.data_ptr(), B, Hq, Hkv, S, d, 1, scale, 2, stream) == 0
+        torch.cuda.synchronize(dev)
+    finally:
+        del os.environ["FA_FWD_TILES"]
+    assert _status(L, stream) & STATUS_WAIT_TIMEOUT
+    assert _status(L, stream) == 0
+    d64 = 64
+    q6, k6, v6, do6 = (x.to(dev) for x in fa_inputs.make_custom(B, Hq, Hkv, S, d64, "bf16", seed=641))
+    out6 = torch.zeros_like(q6)
+    lse6 = torch.zeros(q6.shape[:3], dtype=torch.float32, device=dev)
+    assert L.fa_fwd(q6.data_ptr(), k6.data_ptr(), v6.data_ptr(), out6.data_ptr(), lse6.data_ptr(),
+                    B, Hq, Hkv, S, d64, 1, 1.0 / math.sqrt(d64), 2, stream) == 0
+    torch.cuda.synchronize(dev)
+    assert _status(L, stream) & STATUS_WAIT_TIMEOUT
+    assert _status(L, stream) == 0
+    ref6_out, ref6_lse = fa.attention_forward(q6, k6, v6, True, 1.0 / math.sqrt(d64))
+    dq6, dk6, dv6 = torch.zeros_like(q6), torch.zeros_like(k6), torch.zeros_like(v6)
+    nws6 = L.fa_bwd_workspace_bytes(B, Hq, Hkv, S, d64)
+    ws6 = torch.empty(nws6, dtype=torch.uint8, device=dev)
+    assert L.fa_bwd(q6.data_ptr(), k6.data_ptr(), v6.data_ptr(), ref6_out.data_ptr(),
+                    do6.data_ptr(), ref6_lse.data_ptr(), dq6.data_ptr(), dk6.data_ptr(),
+                    dv6.data_ptr(), B, Hq, Hkv, S, d64, 1, 1.0 / math.sqrt(d64), 2,
+                    ws6.data_ptr(), nws6, stream) == 0
     torch.cuda.synchronize(dev)
     assert _status(L, stream) & STATUS_WAIT_TIMEOUT
     assert _status(L, stream) == 0
